@@ -1,0 +1,197 @@
+"""CPU oracle for the softmax / LayerNorm reduce path (TEST INFRASTRUCTURE).
+
+This package is the checker, not the product.  Only ``tests/``, the smoke
+check in ``__graft_entry__`` and the CPU-baseline leg of ``bench.py`` may
+import it; the library ``transformer_reduce_gb300`` never does, and the two
+share no code.  The arithmetic lives in ``ref_reduce.c`` (plain C, double
+precision, the textbook definitions); this module compiles it with gcc and
+marshals numpy arrays in and out.  Every value that reaches the C code is
+converted exactly to float64 (fp32, fp16 and bf16 values are all doubles),
+so both sides of a parity test see the same numbers.
+
+Sources are cited in ``ref_reduce.c``: the pages "CMU 11-868 L10:
+Accelerating Transformers on GPUs, and Where LightSeq Finds the Time"
+(section "Technique 2", slides 21-24) and "CMU 11-868 HW4：把 Softmax 與
+LayerNorm 寫成 CUDA 融合 kernel" (Problems 1.1-2.2 and the test baseline
+softmax(inp + mask)).
+
+Every function here is pinned by ``tests/test_oracle_pins.py`` to facts that
+do not come from the oracle itself (closed forms, invariants, finite
+differences, library routines); no function is left "parity unpinned".
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "ref_reduce.c")
+_LIB_PATH = os.path.join(_HERE, "libref_reduce.so")
+_lock = threading.Lock()
+_lib = None
+
+# -ffp-contract=off: no fused multiply-add, so x86 and Arm builds round alike.
+_CFLAGS = ["-O2", "-std=c11", "-fPIC", "-shared", "-ffp-contract=off",
+           "-fno-fast-math"]
+
+
+def build(force: bool = False) -> str:
+    """Compile ``ref_reduce.c`` into ``libref_reduce.so`` (gcc); return its path."""
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    cmd = ["gcc", *_CFLAGS, _SRC, "-o", tmp, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        # REF_REDUCE_LIB: a deliberately broken copy of the oracle, built by the
+        # mutation test to show that the pins reject it.
+        lib = ctypes.CDLL(os.environ.get("REF_REDUCE_LIB") or build())
+        dp = ctypes.POINTER(ctypes.c_double)
+        ip = ctypes.POINTER(ctypes.c_int64)
+        i64 = ctypes.c_int64
+        lib.ref_softmax_fw.argtypes = [dp, dp, dp, ip, ip, i64, i64, ctypes.c_int]
+        lib.ref_softmax_fw.restype = None
+        lib.ref_softmax_bw.argtypes = [dp, dp, dp, i64, i64]
+        lib.ref_softmax_bw.restype = None
+        lib.ref_layernorm_fw.argtypes = [dp, dp, dp, dp, dp, dp, i64, i64,
+                                         ctypes.c_double]
+        lib.ref_layernorm_fw.restype = None
+        lib.ref_variance_one_pass.argtypes = [dp, i64, ctypes.c_int]
+        lib.ref_variance_one_pass.restype = ctypes.c_double
+        lib.ref_variance_two_pass.argtypes = [dp, i64]
+        lib.ref_variance_two_pass.restype = ctypes.c_double
+        lib.ref_layernorm_bw_dinp.argtypes = [dp, dp, dp, dp, dp, dp, i64, i64]
+        lib.ref_layernorm_bw_dinp.restype = None
+        lib.ref_layernorm_bw_dgamma_dbeta.argtypes = [dp, dp, dp, dp, dp, dp,
+                                                      i64, i64]
+        lib.ref_layernorm_bw_dgamma_dbeta.restype = None
+        _lib = lib
+        return lib
+
+
+def _f64(a) -> np.ndarray:
+    """Exact conversion of a numpy / torch array to a C-contiguous float64 array."""
+    if a is None:
+        return None
+    if hasattr(a, "detach"):  # torch tensor: widen on the torch side (bf16 has no numpy dtype)
+        import torch
+        a = a.detach().to("cpu", torch.float64).numpy()
+    return np.ascontiguousarray(np.asarray(a, dtype=np.float64))
+
+
+def _ptr(a, ctype=ctypes.c_double):
+    if a is None:
+        return None
+    return a.ctypes.data_as(ctypes.POINTER(ctype))
+
+
+def softmax_fw(x, mask=None, batch=None, query=None, causal=False):
+    """Softmax of (scores + additive mask) over the last axis, per listed row.
+
+    x      : [nrows, Tk] scores (each row one (b, h, i) of a [B,H,Tq,Tk] tensor)
+    mask   : [B, Tk] additive mask or None
+    batch  : [nrows] batch index b of each row (needed with a mask)
+    query  : [nrows] query index i of each row (needed when causal)
+    Returns y [nrows, Tk] float64.
+    """
+    x = _f64(x)
+    nrows, tk = x.shape
+    m = _f64(mask)
+    if m is not None:
+        assert m.ndim == 2 and m.shape[1] == tk
+        batch = np.ascontiguousarray(np.asarray(batch, dtype=np.int64))
+        assert batch.shape == (nrows,)
+        assert batch.size == 0 or (batch.min() >= 0 and batch.max() < m.shape[0])
+    if causal:
+        query = np.ascontiguousarray(np.asarray(query, dtype=np.int64))
+        assert query.shape == (nrows,)
+    y = np.empty_like(x)
+    _load().ref_softmax_fw(_ptr(y), _ptr(x), _ptr(m),
+                           _ptr(batch if m is not None else None, ctypes.c_int64),
+                           _ptr(query if causal else None, ctypes.c_int64),
+                           nrows, tk, int(bool(causal)))
+    return y
+
+
+def softmax_fw_tensor(x4, mask=None, causal=False):
+    """Softmax forward of a whole [B,H,Tq,Tk] tensor; returns [B,H,Tq,Tk] float64."""
+    x4 = _f64(x4)
+    B, H, Tq, Tk = x4.shape
+    rows = np.arange(B * H * Tq, dtype=np.int64)
+    y = softmax_fw(x4.reshape(-1, Tk), mask, batch=rows // (H * Tq),
+                   query=rows % Tq, causal=causal)
+    return y.reshape(B, H, Tq, Tk)
+
+
+def softmax_bw(dy, y):
+    """dx = y * (dy - sum(y * dy)) per row; dy, y [nrows, Tk] -> dx float64."""
+    dy, y = _f64(dy), _f64(y)
+    assert dy.shape == y.shape
+    tk = dy.shape[-1]
+    nrows = dy.size // tk if tk else 0
+    dx = np.empty_like(dy)
+    _load().ref_softmax_bw(_ptr(dx), _ptr(dy), _ptr(y), nrows, tk)
+    return dx
+
+
+def layernorm_fw(x, gamma, beta, eps):
+    """Two-pass LayerNorm; returns (y, mean, rstd) in float64."""
+    x, gamma, beta = _f64(x), _f64(gamma), _f64(beta)
+    rows, n = x.shape
+    assert gamma.shape == (n,) and beta.shape == (n,)
+    y = np.empty_like(x)
+    mean = np.empty(rows)
+    rstd = np.empty(rows)
+    _load().ref_layernorm_fw(_ptr(y), _ptr(mean), _ptr(rstd), _ptr(x),
+                             _ptr(gamma), _ptr(beta), rows, n, float(eps))
+    return y, mean, rstd
+
+
+def variance_one_pass(row, single=False):
+    """mu(x^2) - mu(x)^2 of one row, accumulated in double or float."""
+    row = _f64(row).ravel()
+    return _load().ref_variance_one_pass(_ptr(row), row.size, int(bool(single)))
+
+
+def variance_two_pass(row):
+    """Two-pass population variance of one row."""
+    row = _f64(row).ravel()
+    return _load().ref_variance_two_pass(_ptr(row), row.size)
+
+
+def layernorm_bw_dinp(dy, x, gamma, mean, rstd):
+    """Input gradient of LayerNorm given the saved row statistics."""
+    dy, x, gamma, mean, rstd = map(_f64, (dy, x, gamma, mean, rstd))
+    rows, n = x.shape
+    assert dy.shape == x.shape and gamma.shape == (n,)
+    assert mean.shape == (rows,) and rstd.shape == (rows,)
+    dx = np.empty_like(x)
+    _load().ref_layernorm_bw_dinp(_ptr(dx), _ptr(dy), _ptr(x), _ptr(gamma),
+                                  _ptr(mean), _ptr(rstd), rows, n)
+    return dx
+
+
+def layernorm_bw_dgamma_dbeta(dy, x, mean, rstd):
+    """Column sums dgamma = sum_r dy*xhat, dbeta = sum_r dy; returns float64 pair."""
+    dy, x, mean, rstd = map(_f64, (dy, x, mean, rstd))
+    rows, n = x.shape
+    assert dy.shape == x.shape
+    assert mean.shape == (rows,) and rstd.shape == (rows,)
+    dgamma = np.empty(n)
+    dbeta = np.empty(n)
+    _load().ref_layernorm_bw_dgamma_dbeta(_ptr(dgamma), _ptr(dbeta), _ptr(dy),
+                                          _ptr(x), _ptr(mean), _ptr(rstd), rows, n)
+    return dgamma, dbeta

@@ -1,0 +1,23 @@
+import os
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+
+def pytest_configure(config):
+    config.addinivalue_line(
+        "markers", "gpu: needs a CUDA GPU (sm_103a) and the built libls_reduce.so")
+    config.addinivalue_line(
+        "markers", "slow: full-size workload (still run by default)")
+
+
+@pytest.fixture(scope="session")
+def ref():
+    """The CPU oracle (built on first use)."""
+    import oracle
+    oracle.build()
+    return oracle

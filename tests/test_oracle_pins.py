@@ -1,0 +1,330 @@
+"""Pins of the CPU oracle to facts that do not come from the oracle itself.
+
+Each test checks one oracle function against a closed form, an invariant, a
+central finite difference, or an independent library routine (scipy /
+torch float64 autograd -- the oracle itself is plain C and calls neither).
+Together they are chosen so that a plausible slip in the oracle (a dropped
+term, a wrong sign, an off-by-one in the causal test, the mask indexed by the
+wrong axis, eps outside the square root, N-1 instead of N) fails at least one
+of them; ``test_oracle_mutants.py`` plants such slips and checks exactly that.
+
+Sources: "CMU 11-868 L10: Accelerating Transformers on GPUs, and Where
+LightSeq Finds the Time", "Technique 2" (slides 21-24); "CMU 11-868 HW4：把
+Softmax 與 LayerNorm 寫成 CUDA 融合 kernel", section 題目結構與配分 (Problems
+1.1-2.2, eps = 1e-8) and section 那些「快幾倍」是跟誰比 (softmax(inp + mask)).
+"""
+import math
+
+import numpy as np
+import pytest
+import scipy.special
+import torch
+
+EPS = float(np.float32(1e-8))
+
+
+def _padding_mask(lengths, tk):
+    m = np.zeros((len(lengths), tk))
+    for b, n in enumerate(lengths):
+        m[b, n:] = -np.inf
+    return m
+
+
+# ----------------------------------------------------------------------------
+# softmax forward
+# ----------------------------------------------------------------------------
+
+def test_softmax_fw_plain_rows_match_scipy(ref):
+    rng = np.random.default_rng(11)
+    x = rng.normal(0, 3, size=(37, 53))
+    y = ref.softmax_fw(x)
+    np.testing.assert_allclose(y, scipy.special.softmax(x, axis=-1), rtol=1e-13, atol=1e-16)
+
+
+def test_softmax_fw_additive_mask_uses_batch_axis(ref):
+    # Non-binary additive mask differing per batch entry; H != B so a mask
+    # indexed by head instead of batch disagrees.
+    rng = np.random.default_rng(12)
+    B, H, T = 3, 2, 9
+    x = rng.normal(0, 2, size=(B, H, T, T))
+    mask = rng.normal(0, 1.5, size=(B, T))
+    y = ref.softmax_fw_tensor(x, mask)
+    want = scipy.special.softmax(x + mask[:, None, None, :], axis=-1)
+    np.testing.assert_allclose(y, want, rtol=1e-13, atol=1e-16)
+
+
+def test_softmax_fw_causal_and_padding_zero_pattern(ref):
+    rng = np.random.default_rng(13)
+    B, H, T = 3, 2, 11
+    lengths = [11, 4, 7]
+    x = rng.normal(0, 3, size=(B, H, T, T))
+    mask = _padding_mask(lengths, T)
+    y = ref.softmax_fw_tensor(x, mask, causal=True)
+    for b in range(B):
+        for h in range(H):
+            for i in range(T):
+                valid = np.array([(j <= i) and (j < lengths[b]) for j in range(T)])
+                row = y[b, h, i]
+                # future and padded keys are exactly zero, all others positive
+                assert np.all(row[~valid] == 0.0)
+                assert np.all(row[valid] > 0.0)
+                assert abs(row.sum() - 1.0) < 1e-12
+                np.testing.assert_allclose(
+                    row[valid], scipy.special.softmax(x[b, h, i, valid]), rtol=1e-13)
+
+
+def test_softmax_fw_closed_forms(ref):
+    # two keys: the logistic function of the score difference
+    x = np.array([[0.7, -1.9], [5.0, 5.0], [-30.0, 4.0]])
+    y = ref.softmax_fw(x)
+    for r in range(3):
+        d = x[r, 0] - x[r, 1]
+        assert y[r, 0] == pytest.approx(1.0 / (1.0 + math.exp(-d)), rel=1e-15)
+        assert y[r, 1] == pytest.approx(1.0 / (1.0 + math.exp(d)), rel=1e-14)
+    # equal valid scores: exactly 1/(number of valid keys)
+    x = np.full((1, 8), 2.25)
+    mask = _padding_mask([5], 8)
+    y = ref.softmax_fw(x, mask, batch=[0])
+    assert np.all(y[0, :5] == 0.2) and np.all(y[0, 5:] == 0.0)
+    # a single key gets probability one
+    assert ref.softmax_fw(np.array([[-123.5]]))[0, 0] == 1.0
+
+
+def test_softmax_fw_shift_invariance_and_no_overflow(ref):
+    rng = np.random.default_rng(14)
+    x = rng.normal(0, 3, size=(5, 31))
+    y0 = ref.softmax_fw(x)
+    y1 = ref.softmax_fw(x + 1000.0)   # exp(1000) overflows without the max shift
+    assert np.all(np.isfinite(y1))
+    np.testing.assert_allclose(y1, y0, rtol=1e-10, atol=1e-15)
+
+
+def test_softmax_fw_fully_masked_row_is_zero(ref):
+    x = np.array([[1.0, 2.0, 3.0], [1.0, 2.0, 3.0]])
+    mask = np.array([[-np.inf, -np.inf, -np.inf], [0.0, -np.inf, 0.0]])
+    y = ref.softmax_fw(x, mask, batch=[0, 1])
+    assert np.all(y[0] == 0.0)
+    np.testing.assert_allclose(y[1], [1 / (1 + math.e ** 2), 0.0, math.e ** 2 / (1 + math.e ** 2)],
+                               rtol=1e-15)
+
+
+def test_softmax_fw_empty(ref):
+    assert ref.softmax_fw(np.zeros((0, 7))).shape == (0, 7)
+    assert ref.softmax_fw(np.zeros((3, 0))).shape == (3, 0)
+
+
+# ----------------------------------------------------------------------------
+# softmax backward
+# ----------------------------------------------------------------------------
+
+@pytest.mark.parametrize("shape,causal,lengths", [
+    ((1, 2, 3, 3), True, None),
+    ((1, 1, 5, 5), True, [3]),
+    ((2, 1, 4, 4), False, [2, 4]),
+])
+def test_softmax_bw_central_differences(ref, shape, causal, lengths):
+    rng = np.random.default_rng(21)
+    B, H, Tq, Tk = shape
+    x = rng.normal(0, 1, size=shape)
+    dy = rng.normal(0, 1, size=shape)
+    mask = _padding_mask(lengths, Tk) if lengths else None
+
+    def loss(xx):
+        return float(np.sum(dy * ref.softmax_fw_tensor(xx, mask, causal=causal)))
+
+    y = ref.softmax_fw_tensor(x, mask, causal=causal)
+    dx = ref.softmax_bw(dy.reshape(-1, Tk), y.reshape(-1, Tk)).reshape(shape)
+    h = 1e-6
+    fd = np.zeros(shape)
+    for idx in np.ndindex(shape):
+        xp, xm = x.copy(), x.copy()
+        xp[idx] += h
+        xm[idx] -= h
+        fd[idx] = (loss(xp) - loss(xm)) / (2 * h)
+    scale = np.max(np.abs(fd))
+    assert np.max(np.abs(dx - fd)) <= 1e-6 * scale
+
+
+def test_softmax_bw_matches_torch_autograd(ref):
+    rng = np.random.default_rng(22)
+    B, H, T = 2, 3, 6
+    x = torch.tensor(rng.normal(0, 2, size=(B, H, T, T)), requires_grad=True)
+    dy = torch.tensor(rng.normal(0, 1, size=(B, H, T, T)))
+    mask = torch.tensor(_padding_mask([6, 3], T))
+    causal = torch.triu(torch.full((T, T), -math.inf, dtype=torch.float64), diagonal=1)
+    y = torch.softmax(x + mask[:, None, None, :] + causal, dim=-1)
+    y.backward(dy)
+    yo = ref.softmax_fw_tensor(x.detach().numpy(), mask.numpy(), causal=True)
+    np.testing.assert_allclose(yo, y.detach().numpy(), rtol=1e-13, atol=1e-16)
+    dx = ref.softmax_bw(dy.numpy().reshape(-1, T), yo.reshape(-1, T)).reshape(B, H, T, T)
+    np.testing.assert_allclose(dx, x.grad.numpy(), rtol=1e-12, atol=1e-15)
+
+
+def test_softmax_bw_invariants(ref):
+    rng = np.random.default_rng(23)
+    y = scipy.special.softmax(rng.normal(0, 2, size=(9, 17)), axis=-1)
+    dy = rng.normal(0, 1, size=(9, 17))
+    dx = ref.softmax_bw(dy, y)
+    np.testing.assert_allclose(dx.sum(axis=-1), 0.0, atol=1e-14)
+    # a constant upstream gradient has no effect on a normalised output
+    dx_c = ref.softmax_bw(np.full((9, 17), 3.5), y)
+    np.testing.assert_allclose(dx_c, 0.0, atol=1e-14)
+    # zero probabilities give zero gradient whatever dy is
+    y0 = y.copy()
+    y0[:, :4] = 0.0
+    assert np.all(ref.softmax_bw(dy, y0)[:, :4] == 0.0)
+
+
+# ----------------------------------------------------------------------------
+# LayerNorm forward
+# ----------------------------------------------------------------------------
+
+def test_layernorm_fw_matches_torch(ref):
+    rng = np.random.default_rng(31)
+    x = rng.normal(1, 2, size=(13, 96))
+    g = rng.uniform(0.5, 1.5, size=96)
+    b = rng.normal(0, 0.1, size=96)
+    for eps in (EPS, 0.25):   # a large eps makes "eps inside the root" visible
+        y, mean, rstd = ref.layernorm_fw(x, g, b, eps)
+        want = torch.nn.functional.layer_norm(
+            torch.tensor(x), (96,), torch.tensor(g), torch.tensor(b), eps)
+        np.testing.assert_allclose(y, want.numpy(), rtol=1e-12, atol=1e-13)
+        np.testing.assert_allclose(mean, x.mean(axis=1), rtol=1e-14)
+        np.testing.assert_allclose(rstd, 1 / np.sqrt(x.var(axis=1) + eps), rtol=1e-13)
+
+
+def test_layernorm_fw_unit_affine_invariants(ref):
+    rng = np.random.default_rng(32)
+    x = rng.normal(0, 1, size=(64, 128))
+    y, mean, rstd = ref.layernorm_fw(x, np.ones(128), np.zeros(128), EPS)
+    np.testing.assert_allclose(y.mean(axis=1), 0.0, atol=1e-12)
+    var = x.var(axis=1)
+    np.testing.assert_allclose(y.var(axis=1), var / (var + EPS), rtol=1e-12)
+    # affine invariance: y(a x + c) = y(x) up to the eps term (a > 0)
+    y2, _, _ = ref.layernorm_fw(3.0 * x - 7.0, np.ones(128), np.zeros(128), EPS)
+    np.testing.assert_allclose(y2, y, rtol=1e-7, atol=1e-7)
+
+
+def test_layernorm_fw_constant_row(ref):
+    # dyadic constants: the mean is exact, so x - mean is exactly 0
+    x = np.full((2, 40), 0.375)
+    x[1] = -3.0
+    g = np.linspace(0.5, 1.5, 40)
+    b = np.linspace(-0.2, 0.2, 40)
+    y, mean, rstd = ref.layernorm_fw(x, g, b, EPS)
+    assert np.all(y == b)
+    np.testing.assert_allclose(rstd, 1 / math.sqrt(EPS), rtol=1e-12)
+    assert list(mean) == [0.375, -3.0]
+
+
+def test_layernorm_fw_hand_example(ref):
+    # x = [1,2,3,4]: mu = 2.5, population var = 1.25 (not 5/3)
+    y, mean, rstd = ref.layernorm_fw(np.array([[1.0, 2, 3, 4]]), np.ones(4), np.zeros(4), 0.0)
+    assert mean[0] == 2.5
+    assert rstd[0] == pytest.approx(1 / math.sqrt(1.25), rel=1e-15)
+    np.testing.assert_allclose(y[0], np.array([-1.5, -0.5, 0.5, 1.5]) / math.sqrt(1.25),
+                               rtol=1e-15)
+
+
+def test_one_pass_vs_two_pass_variance(ref):
+    """The slide-21 rewrite agrees with the definition; fp32 accumulation loses digits."""
+    assert ref.variance_one_pass([1.0, 2, 3, 4]) == 1.25
+    assert ref.variance_two_pass([1.0, 2, 3, 4]) == 1.25
+    rng = np.random.default_rng(33)
+    worst_d, worst_f = 0.0, 0.0
+    for n in (8, 128, 768, 8192):
+        for mu, sd in ((0.0, 1.0), (1.0, 2.0)):
+            row = rng.normal(mu, sd, size=n).astype(np.float32).astype(np.float64)
+            v2 = ref.variance_two_pass(row)
+            assert v2 == pytest.approx(np.var(row), rel=1e-13)
+            worst_d = max(worst_d, abs(ref.variance_one_pass(row) - v2) / v2)
+            worst_f = max(worst_f, abs(ref.variance_one_pass(row, single=True) - v2) / v2)
+    assert worst_d < 1e-12            # same value in double
+    assert 1e-9 < worst_f < 1e-3      # float accumulation: visibly fp32, still close
+    # a large common offset makes the float form cancel catastrophically
+    row = 1.0e4 + rng.normal(0, 1, size=1024)
+    v2 = ref.variance_two_pass(row)
+    assert abs(ref.variance_one_pass(row, single=True) - v2) / v2 > 0.1
+
+
+# ----------------------------------------------------------------------------
+# LayerNorm backward
+# ----------------------------------------------------------------------------
+
+@pytest.mark.parametrize("rows,n", [(3, 5), (4, 8)])
+def test_layernorm_dinp_central_differences(ref, rows, n):
+    rng = np.random.default_rng(41)
+    x = rng.normal(1, 2, size=(rows, n))
+    g = rng.uniform(0.5, 1.5, size=n)
+    b = rng.normal(0, 0.1, size=n)
+    dy = rng.normal(0, 1, size=(rows, n))
+    eps = 1e-3
+
+    def loss(xx):
+        return float(np.sum(dy * ref.layernorm_fw(xx, g, b, eps)[0]))
+
+    _, mean, rstd = ref.layernorm_fw(x, g, b, eps)
+    dx = ref.layernorm_bw_dinp(dy, x, g, mean, rstd)
+    h = 1e-6
+    fd = np.zeros_like(x)
+    for idx in np.ndindex(x.shape):
+        xp, xm = x.copy(), x.copy()
+        xp[idx] += h
+        xm[idx] -= h
+        fd[idx] = (loss(xp) - loss(xm)) / (2 * h)
+    assert np.max(np.abs(dx - fd)) <= 1e-6 * np.max(np.abs(fd))
+
+
+def test_layernorm_bw_matches_torch_autograd(ref):
+    rng = np.random.default_rng(42)
+    rows, n = 7, 24
+    x = torch.tensor(rng.normal(1, 2, size=(rows, n)), requires_grad=True)
+    g = torch.tensor(rng.uniform(0.5, 1.5, size=n), requires_grad=True)
+    b = torch.tensor(rng.normal(0, 0.1, size=n), requires_grad=True)
+    dy = torch.tensor(rng.normal(0, 1, size=(rows, n)))
+    torch.nn.functional.layer_norm(x, (n,), g, b, EPS).backward(dy)
+    _, mean, rstd = ref.layernorm_fw(x.detach().numpy(), g.detach().numpy(),
+                                     b.detach().numpy(), EPS)
+    dx = ref.layernorm_bw_dinp(dy.numpy(), x.detach().numpy(), g.detach().numpy(), mean, rstd)
+    np.testing.assert_allclose(dx, x.grad.numpy(), rtol=1e-11, atol=1e-12)
+    dg, db = ref.layernorm_bw_dgamma_dbeta(dy.numpy(), x.detach().numpy(), mean, rstd)
+    np.testing.assert_allclose(dg, g.grad.numpy(), rtol=1e-11, atol=1e-12)
+    np.testing.assert_allclose(db, b.grad.numpy(), rtol=1e-12, atol=1e-13)
+
+
+def test_layernorm_dinp_row_sum_is_zero(ref):
+    rng = np.random.default_rng(43)
+    x = rng.normal(1, 2, size=(16, 33))
+    g = rng.uniform(0.5, 1.5, size=33)
+    _, mean, rstd = ref.layernorm_fw(x, g, np.zeros(33), EPS)
+    dx = ref.layernorm_bw_dinp(rng.normal(size=(16, 33)), x, g, mean, rstd)
+    np.testing.assert_allclose(dx.sum(axis=1), 0.0, atol=1e-12)
+
+
+def test_layernorm_dgamma_dbeta_central_differences(ref):
+    rng = np.random.default_rng(44)
+    rows, n = 6, 5
+    x = rng.normal(0, 1, size=(rows, n))
+    g = rng.uniform(0.5, 1.5, size=n)
+    b = rng.normal(0, 0.1, size=n)
+    dy = rng.normal(0, 1, size=(rows, n))
+    _, mean, rstd = ref.layernorm_fw(x, g, b, EPS)
+    dg, db = ref.layernorm_bw_dgamma_dbeta(dy, x, mean, rstd)
+    h = 1e-6
+    for j in range(n):
+        gp, gm = g.copy(), g.copy()
+        gp[j] += h
+        gm[j] -= h
+        fd = (np.sum(dy * ref.layernorm_fw(x, gp, b, EPS)[0])
+              - np.sum(dy * ref.layernorm_fw(x, gm, b, EPS)[0])) / (2 * h)
+        assert dg[j] == pytest.approx(fd, rel=1e-6, abs=1e-8)
+    # dbeta is the plain column sum of dy
+    np.testing.assert_allclose(db, dy.sum(axis=0), rtol=1e-14)
+
+
+def test_layernorm_empty_rows(ref):
+    y, mean, rstd = ref.layernorm_fw(np.zeros((0, 4)), np.ones(4), np.zeros(4), EPS)
+    assert y.shape == (0, 4) and mean.shape == (0,)
+    dg, db = ref.layernorm_bw_dgamma_dbeta(np.zeros((0, 4)), np.zeros((0, 4)),
+                                           np.zeros(0), np.zeros(0))
+    assert np.all(dg == 0.0) and np.all(db == 0.0)
