@@ -1,0 +1,418 @@
+#!/usr/bin/env python3
+"""Benchmark of the softmax / LayerNorm reduce path on GB300.
+
+One step = one pass of the whole hot path of a Transformer-big encoder layer
+(attention softmax [32,16,512,512] bf16 with a padding mask, two LayerNorms
+[16384,1024] bf16; forward and backward; ten kernel launches) through the C
+ABI of libls_reduce.so, inputs resident in HBM.  The metric is whole-job
+algorithmic HBM GB/s (bytes the method must move / time), with rows/s and the
+roofline fraction of the dominant kernel beside it.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+With N > 1 (launched by torch.distributed.run) every rank runs its own
+replica of the pass on its own GPU (the rows are independent; there is no
+data-path collective); the job time is the maximum over ranks.
+
+--impl reference times the CPU oracle (fp64 C, one host core) on a bounded
+row sample of the same workload; it is a deliberately slow baseline.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "softmax & LayerNorm fwd+bwd HBM GB/s (% of GB300 peak) and rows/s"
+WORKLOAD = ("encoder_big: attention softmax fwd+bwd [B=32,H=16,T=512,T=512] bf16, padding "
+            "mask (valid length U[256,512]), no causal; two LayerNorm fwd+bwd (dinp, "
+            "dgamma/dbeta) [16384,1024] bf16, eps=1e-8; one stream, pre-LN layer order")
+FALLBACK_HBM_GBS = 6800.0
+DOMINANT = "softmax_bw"
+# ncu summary with the dominant kernel's DRAM bytes per launch (see profiles/)
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "softmax_bw_encoder_big.txt")
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing (one process per GPU; only a barrier and a max)
+# ---------------------------------------------------------------------------
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def init_dist(world, backend):
+    if world > 1 and not torch.distributed.is_initialized():
+        torch.distributed.init_process_group(backend=backend)
+
+
+def barrier(world):
+    if world > 1:
+        torch.distributed.barrier()
+
+
+def max_over_ranks(value: float, world: int) -> float:
+    """The largest value any rank holds (the job time is the slowest rank's)."""
+    if world <= 1:
+        return value
+    dev = "cuda" if torch.distributed.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(value: float, world: int) -> float:
+    if world <= 1:
+        return value
+    dev = "cuda" if torch.distributed.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.SUM)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------
+# peaks, clocks, ncu traffic
+# ---------------------------------------------------------------------------
+
+def hbm_peak():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled every 200 ms."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.gpu = gpu_index
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={gpu_index}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def csrc_digest() -> str:
+    h = hashlib.sha256()
+    d = os.path.join(ROOT, "transformer_reduce_gb300", "csrc")
+    for fn in sorted(os.listdir(d)):
+        with open(os.path.join(d, fn), "rb") as f:
+            h.update(fn.encode())
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic():
+    """DRAM bytes per launch of the dominant kernel from the committed ncu
+    summary, or None when missing or taken on different kernel sources."""
+    try:
+        text = open(TRAFFIC_FILE).read()
+    except OSError:
+        return None
+    m = re.search(r"^traffic_bytes_per_launch:\s*(\d+)\s+csrc_sha=(\w+)", text, re.M)
+    if not m or m.group(2) != csrc_digest():
+        return None
+    return int(m.group(1))
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle baseline (bounded row sample of the same workload)
+# ---------------------------------------------------------------------------
+
+class OracleSample:
+    """Row sample of the encoder pass, staged as float64 host arrays.
+
+    sm_case / sm_inputs: the softmax case and its tensors (scores, mask, dout,
+    lengths); ln: list of (LayerNormCase, inputs dict with x, gamma, beta, dy).
+    """
+
+    def __init__(self, sm_case, sm_inputs, ln, softmax_frac=32, ln_frac=4):
+        import oracle
+        from transformer_reduce_gb300 import traffic
+        oracle.build()
+        self.oracle = oracle
+        s = sm_case
+        rows = np.arange(0, s.rows, softmax_frac, dtype=np.int64)
+        flat = sm_inputs["scores"].reshape(-1, s.T)
+        idx = torch.from_numpy(rows).to(flat.device)
+        self.x = flat.index_select(0, idx).double().cpu().numpy()
+        self.dy = sm_inputs["dout"].reshape(-1, s.T).index_select(0, idx).double().cpu().numpy()
+        mask = sm_inputs["mask"]
+        self.mask = None if mask is None else mask.double().cpu().numpy()
+        self.batch = rows // (s.H * s.T)
+        self.query = rows % s.T
+        self.causal = s.causal
+        frac_s = len(rows) / s.rows
+        self.bytes = (traffic.softmax_fw_bytes(s.B, s.H, s.T, sm_inputs["lengths"], s.causal,
+                                               s.dtype, mask is not None)
+                      + traffic.softmax_bw_bytes(s.B, s.H, s.T, s.dtype)) * frac_s
+        self.ln = []
+        for c, li in ln:
+            n = c.rows // ln_frac
+            self.ln.append((li["x"][:n].double().cpu().numpy(), li["gamma"].double().cpu().numpy(),
+                            li["beta"].double().cpu().numpy(), li["dy"][:n].double().cpu().numpy(),
+                            c))
+            self.bytes += (traffic.layernorm_fw_bytes(n, c.hidden, c.dtype)
+                           + traffic.layernorm_dinp_bytes(n, c.hidden, c.dtype)
+                           + traffic.layernorm_dgdb_bytes(n, c.hidden, c.dtype))
+        self.description = (f"every {softmax_frac}th softmax row ({len(rows)} of {s.rows}) fw+bw, "
+                            f"first 1/{ln_frac} of each LayerNorm's rows fw+dinp+dgamma/dbeta; "
+                            "inputs pre-staged as float64 host arrays; 1 host thread")
+
+    @classmethod
+    def from_path(cls, path, **kw):
+        sm_inputs = {"scores": path.scores, "dout": path.dprobs, "mask": path.mask,
+                     "lengths": path.lengths}
+        ln = [(b.case, {"x": b.x, "gamma": b.gamma, "beta": b.beta, "dy": b.dy}) for b in path.ln]
+        return cls(path.sm, sm_inputs, ln, **kw)
+
+    def run(self):
+        o = self.oracle
+        y = o.softmax_fw(self.x, self.mask, batch=self.batch, query=self.query, causal=self.causal)
+        o.softmax_bw(self.dy, y)
+        for x, g, b, dy, c in self.ln:
+            _, m, r = o.layernorm_fw(x, g, b, c.eps)
+            o.layernorm_bw_dinp(dy, x, g, m, r)
+            o.layernorm_bw_dgamma_dbeta(dy, x, m, r)
+
+    def time(self, min_seconds=10.0, max_passes=1000):
+        self.run()  # first touch of the output buffers is not timed
+        n, t0 = 0, time.perf_counter()
+        while True:
+            self.run()
+            n += 1
+            el = time.perf_counter() - t0
+            if el >= min_seconds or n >= max_passes:
+                return el / n
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+
+def run_ours(args):
+    world, rank, local = dist_env()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py: no CUDA device (the library has no CPU path)")
+    torch.cuda.set_device(local)
+    init_dist(world, "nccl")
+    from transformer_reduce_gb300 import build, workloads
+    build.build()
+    from transformer_reduce_gb300.layer_path import LayerReducePath
+    dev = torch.device("cuda", local)
+    path = LayerReducePath(workloads.ENCODER_BIG["softmax"], workloads.ENCODER_BIG["layernorm"],
+                           device=dev)
+    stream = torch.cuda.Stream(dev)
+    step_bytes = path.step_bytes()
+    kbytes = path.kernel_bytes()
+    launches_per_step = sum(2 if n == "ln_dgdb" else 1 for n, _ in path.sequence())
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+
+    clocks = ClockSampler(local)
+    for _ in range(args.warmup):
+        path.run(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    timers = {}
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(args.steps):
+        path.run(stream, timers=timers)
+    t1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    clk = clocks.stop()
+    elapsed_s = t0.elapsed_time(t1) / 1e3
+    job_s = max_over_ranks(elapsed_s, world)
+    total_bytes = sum_over_ranks(step_bytes * args.steps, world)
+    value = total_bytes / job_s / 1e9
+
+    peak, peak_src = hbm_peak()
+    kernels = {}
+    for name, pairs in timers.items():
+        ms = [a.elapsed_time(b) for a, b in pairs]
+        per_launch = kbytes[name]
+        calls_per_step = len(per_launch)
+        avg_ms = sum(ms) / len(ms)
+        bytes_per_call = sum(per_launch) / calls_per_step
+        gbs = bytes_per_call / (avg_ms / 1e3) / 1e9
+        kernels[name] = {"calls_per_step": calls_per_step, "avg_ms": round(avg_ms, 5),
+                         "bytes_per_call": int(bytes_per_call), "gbs": round(gbs, 1),
+                         "frac_of_peak": round(gbs / peak, 4)}
+    dom = kernels[DOMINANT]
+    traffic = ncu_traffic()
+    roofline = {"bound": "hbm", "kernel": "softmax_bw_vec<bf16,32,2>", "achieved": dom["gbs"],
+                "peak": peak, "peak_source": peak_src, "unit": "GB/s",
+                "frac": round(dom["gbs"] / peak, 4), "traffic": traffic,
+                "algorithmic_bytes": dom["bytes_per_call"]}
+
+    # end to end: pinned host inputs -> device, the pass, outputs -> pinned host
+    e2e_steps = max(3, min(args.steps // 20, 30))
+    path.host_buffers()
+    path.upload(stream)
+    path.run(stream)
+    path.download(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        path.upload(stream)
+        path.run(stream)
+        path.download(stream)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    e2e_s = max_over_ranks(e0.elapsed_time(e1) / 1e3, world)
+    e2e_value = sum_over_ranks(step_bytes * e2e_steps, world) / e2e_s / 1e9
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        sample = OracleSample.from_path(path)
+        per_pass = sample.time(min_seconds=args.cpu_seconds)
+        cpu = {"value": round(sample.bytes / per_pass / 1e9, 4), "unit": "GB/s", "cores": 1,
+               "kind": "oracle", "sample": sample.description,
+               "seconds_per_sample_pass": round(per_pass, 4)}
+
+    rows = path.rows()
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(job_s / args.steps * 1e3, 5), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "storage": "bf16", "parallelism": "replicas",
+                       "l2": f"inputs larger than L2 (pass moves {step_bytes / 1e9:.2f} GB; "
+                             f"L2 {l2 / 1e6:.0f} MB); no flush"},
+            "pct_of_peak": round(100 * value / world / peak, 2),
+            "rows_per_s": {k: round(world * v * args.steps / job_s) for k, v in rows.items()},
+            "bytes_per_step": step_bytes,
+            "kernels": kernels,
+            "roofline": roofline,
+            "cpu_baseline": cpu,
+            "e2e": {"value": round(e2e_value, 1), "unit": "GB/s",
+                    "h2d_bytes_per_step": path.h2d_bytes(), "d2h_bytes_per_step": path.d2h_bytes(),
+                    "steps": e2e_steps, "ms_per_step": round(e2e_s / e2e_steps * 1e3, 4)},
+            "clocks": clk,
+            "gpu_launches": launches_per_step * args.steps,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+# ---------------------------------------------------------------------------
+# reference arm: the CPU oracle
+# ---------------------------------------------------------------------------
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return  # rank 0 alone runs the CPU reference
+    from transformer_reduce_gb300 import workloads
+    # inputs are drawn by torch's generator (on the GPU when there is one, for
+    # speed); no kernel of this repository runs in this arm
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    sm_case = workloads.ENCODER_BIG["softmax"]
+    ln_cases = workloads.ENCODER_BIG["layernorm"]
+    sm_inputs = workloads.softmax_inputs(sm_case, device=dev)
+    ln = [(c, workloads.layernorm_inputs(c, device=dev)) for c in ln_cases]
+    sample = OracleSample(sm_case, sm_inputs, ln, softmax_frac=64, ln_frac=8)
+    del sm_inputs, ln
+    sample.run()
+    for _ in range(args.warmup):
+        sample.run()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        sample.run()
+    el = time.perf_counter() - t0
+    value = sample.bytes * args.steps / el / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(el / args.steps * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "storage": "bf16", "parallelism": "single host thread",
+                   "sample": sample.description},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": sample.description},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0,
+                    help="minimum host time spent timing the CPU oracle sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,189 @@
+/*
+ * ls_reduce.h -- C ABI of libls_reduce.so: fused softmax and LayerNorm reduce
+ * kernels of a Transformer layer (forward and backward) for NVIDIA GB300
+ * (sm_103a).
+ *
+ * The operations are the LightSeq-style reduce kernels described on the pages
+ *   "CMU 11-868 L10: Accelerating Transformers on GPUs, and Where LightSeq
+ *    Finds the Time", section "Technique 2: rewrite the formula, drop a
+ *    synchronization" (slides 21-26), and
+ *   "CMU 11-868 HW4：把 Softmax 與 LayerNorm 寫成 CUDA 融合 kernel",
+ *    section 題目結構與配分 (Problems 1.1, 1.2, 2.1, 2.2).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Pointers named as device buffers must be CUDA device (or managed) memory
+ *    owned by the caller.  The library never allocates, frees or
+ *    synchronises; it only enqueues kernels on `stream`.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
+ *    stream).  All work is asynchronous with respect to the host.
+ *  - Tensors are dense, row-major, with the last dimension contiguous.
+ *  - Storage dtype `dt` applies to every `void*` tensor of a call (scores,
+ *    mask, gamma, beta, activations and their gradients).  Arithmetic is FP32
+ *    for every storage dtype; 16-bit outputs are rounded to nearest-even.
+ *    LayerNorm statistics (mean, rstd) and the gamma/beta gradients are
+ *    always FP32.
+ *  - Pointers must be aligned to their element size.  Buffers that are also
+ *    16-byte aligned, with a row length in bytes that is a multiple of 16,
+ *    take the 128-bit vector path; all others take a scalar path of the same
+ *    kernel family (same results, lower bandwidth).  There is no CPU path.
+ *  - A zero-sized problem (no rows, or an empty row for softmax) is a valid
+ *    no-op, except where stated.  Negative sizes, NULL required pointers,
+ *    unsupported dtypes and inconsistent shapes are rejected on the host
+ *    before anything is launched; nothing is written in that case.
+ *  - Return value: LS_OK once the kernels are enqueued.  A launch failure
+ *    reported by the CUDA runtime is LS_ERR_CUDA.  Faults that happen while
+ *    the kernels run surface at the caller's next synchronisation, as for any
+ *    CUDA work.
+ */
+#ifndef LS_REDUCE_H
+#define LS_REDUCE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum ls_dtype {
+    LS_F32 = 0,  /* IEEE binary32 */
+    LS_F16 = 1,  /* IEEE binary16 */
+    LS_BF16 = 2  /* bfloat16 */
+} ls_dtype;
+
+typedef enum ls_status {
+    LS_OK = 0,
+    LS_ERR_INVALID_ARG = 1,  /* NULL pointer, negative size, inconsistent shape */
+    LS_ERR_UNSUPPORTED = 2,  /* unknown dtype, or a size beyond the limits below */
+    LS_ERR_MISALIGNED = 3,   /* pointer not aligned to its element size */
+    LS_ERR_WORKSPACE = 4,    /* workspace missing or smaller than required */
+    LS_ERR_CUDA = 5          /* the CUDA runtime rejected a launch */
+} ls_status;
+
+/* Largest row length (Tk for softmax, hidden for LayerNorm) accepted. */
+#define LS_MAX_ROW_LENGTH ((int64_t)1 << 30)
+
+/*
+ * Attention softmax forward ("Problem 1.1" of the HW4 page; slides 23-26 of
+ * the L10 page).  For every row (b, h, i) of the score tensor:
+ *     z_j = -inf                       if causal and j > i  (future key)
+ *     z_j = inp[b,h,i,j] + mask[b,j]   otherwise
+ *     out[b,h,i,j] = exp(z_j - max_k z_k) / sum_k exp(z_k - max_k z_k)
+ * A row whose every key is -inf is written as zeros.
+ *
+ *   out   [B,H,Tq,Tk] dt, device, written.  May equal `inp` (in place).
+ *   inp   [B,H,Tq,Tk] dt, device, read.  Scores are expected to be finite.
+ *   mask  [B,Tk] dt additive mask (0 = keep, -inf = padded key), device,
+ *         read; NULL means no mask.  Shared by all heads and queries of a
+ *         batch entry.  Keys whose mask is -inf are not read from `inp`.
+ *   causal  nonzero: mask future keys j > i; requires Tq == Tk.
+ * Errors: LS_ERR_INVALID_ARG for NULL out/inp with a non-empty problem,
+ * negative sizes, or causal with Tq != Tk; LS_ERR_UNSUPPORTED for Tk beyond
+ * LS_MAX_ROW_LENGTH or an unknown dtype.
+ */
+ls_status ls_softmax_fw(void *out, const void *inp, const void *mask,
+                        int64_t B, int64_t H, int64_t Tq, int64_t Tk,
+                        int causal, ls_dtype dt, void *stream);
+
+/*
+ * Attention softmax backward ("Problem 1.2" of the HW4 page).  For every
+ * row:  dinp_j = out_j * (dout_j - sum_k out_k * dout_k),
+ * the vector-Jacobian product of the forward softmax at its output `out_fw`.
+ * Masked and future keys need no mask argument: their forward output is 0.
+ *
+ *   dinp    [B,H,Tq,Tk] dt, device, written.  May equal `dout`.
+ *   dout    [B,H,Tq,Tk] dt, device, read (gradient of the softmax output).
+ *   out_fw  [B,H,Tq,Tk] dt, device, read (the forward output).
+ * Errors as for ls_softmax_fw (no causal/mask arguments here).
+ */
+ls_status ls_softmax_bw(void *dinp, const void *dout, const void *out_fw,
+                        int64_t B, int64_t H, int64_t Tq, int64_t Tk,
+                        ls_dtype dt, void *stream);
+
+/*
+ * LayerNorm forward ("Problem 2.1" of the HW4 page; slide 21 of the L10
+ * page).  For every row of x [rows, hidden], the mean and variance come from
+ * ONE fused reduction of the two sums sum(x') and sum(x'^2), x' = x - x_0
+ * (x_0 the row's first element; the variance is shift-invariant and the
+ * shift keeps the one-pass form exact for constant rows):
+ *     mu   = x_0 + mean(x'),   var = max(mean(x'^2) - mean(x')^2, 0)
+ *     rstd = 1 / sqrt(var + eps)
+ *     y_j  = (x_j - mu) * rstd * gamma_j + beta_j
+ *
+ *   y      [rows, hidden] dt, device, written.
+ *   mean   [rows] float32, device, written (the saved mu).
+ *   rstd   [rows] float32, device, written (the saved 1/sqrt(var + eps)).
+ *   x      [rows, hidden] dt, device, read.
+ *   gamma, beta  [hidden] dt, device, read.
+ *   eps    added to the variance inside the square root (the pages use 1e-8).
+ * Errors: LS_ERR_INVALID_ARG for NULL pointers with rows > 0, negative rows,
+ * hidden < 1, or eps < 0 / not finite; LS_ERR_UNSUPPORTED for hidden beyond
+ * LS_MAX_ROW_LENGTH or an unknown dtype.
+ */
+ls_status ls_layernorm_fw(void *y, float *mean, float *rstd, const void *x,
+                          const void *gamma, const void *beta, int64_t rows,
+                          int64_t hidden, float eps, ls_dtype dt, void *stream);
+
+/*
+ * LayerNorm backward, input gradient ("Problem 2.2" of the HW4 page; slide
+ * 22 of the L10 page: two sums computed in parallel, then elementwise work).
+ * With xhat = (x - mean) * rstd and g = gamma * dy, per row:
+ *     S1 = sum_j g_j,   S2 = sum_j g_j * xhat_j      (one fused reduction)
+ *     dx_j = rstd * (g_j - S1 / hidden - xhat_j * S2 / hidden)
+ *
+ *   dx     [rows, hidden] dt, device, written.  May equal `dy`.
+ *   dy     [rows, hidden] dt, device, read (gradient of y).
+ *   x      [rows, hidden] dt, device, read (the forward input).
+ *   gamma  [hidden] dt, device, read.
+ *   mean, rstd  [rows] float32, device, read (as saved by ls_layernorm_fw).
+ * Errors as for ls_layernorm_fw.
+ */
+ls_status ls_layernorm_bw_dinp(void *dx, const void *dy, const void *x,
+                               const void *gamma, const float *mean,
+                               const float *rstd, int64_t rows, int64_t hidden,
+                               ls_dtype dt, void *stream);
+
+/*
+ * Bytes of device workspace ls_layernorm_bw_dgamma_dbeta needs for a
+ * [rows, hidden] problem (the same for every dtype).  Returns 0 for
+ * rows <= 0 or hidden <= 0.  Host-only; launches nothing.
+ */
+size_t ls_layernorm_bw_dgamma_dbeta_workspace_size(int64_t rows, int64_t hidden);
+
+/*
+ * LayerNorm backward, gamma and beta gradients ("Problem 2.2" of the HW4
+ * page: the cross-row kernel).  Column sums over all rows:
+ *     dgamma_j = sum_r dy_rj * (x_rj - mean_r) * rstd_r
+ *     dbeta_j  = sum_r dy_rj
+ * computed in a fixed order that depends only on (rows, hidden): the result
+ * is bitwise reproducible from run to run and GPU to GPU.  With rows == 0 the
+ * outputs are set to zero.
+ *
+ *   dgamma, dbeta  [hidden] float32, device, written (overwritten, not
+ *                  accumulated into).
+ *   dy, x          [rows, hidden] dt, device, read.
+ *   mean, rstd     [rows] float32, device, read.
+ *   workspace      device scratch of at least
+ *                  ls_layernorm_bw_dgamma_dbeta_workspace_size(rows, hidden)
+ *                  bytes, 16-byte aligned; its contents on entry do not
+ *                  matter and are left undefined.  May be NULL when that size
+ *                  is 0.  Calls that overlap on the GPU must not share it.
+ * Errors as for ls_layernorm_fw, plus LS_ERR_WORKSPACE when the workspace is
+ * NULL, too small or not 16-byte aligned.
+ */
+ls_status ls_layernorm_bw_dgamma_dbeta(float *dgamma, float *dbeta,
+                                       const void *dy, const void *x,
+                                       const float *mean, const float *rstd,
+                                       int64_t rows, int64_t hidden,
+                                       void *workspace, size_t workspace_bytes,
+                                       ls_dtype dt, void *stream);
+
+/* Static, human-readable name of a status code (never NULL). */
+const char *ls_status_string(ls_status s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LS_REDUCE_H */

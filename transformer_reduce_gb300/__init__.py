@@ -1,0 +1,142 @@
+"""transformer_reduce_gb300 -- fused softmax and LayerNorm reduce kernels of a
+Transformer layer, forward and backward, for NVIDIA GB300 (sm_103a).
+
+The compute is hand-written CUDA in ``libls_reduce.so`` behind a C ABI
+(``include/ls_reduce.h``).  ``transformer_reduce_gb300._lib`` mirrors that ABI
+one-for-one (raw pointers); the functions below are the PyTorch-facing
+convenience layer: they check shapes, allocate outputs with torch, and pass
+pointers and the current CUDA stream to the library.  There is no fallback:
+if the library is missing or a call fails, they raise.
+"""
+from __future__ import annotations
+
+from ._lib import (LS_BF16, LS_ERR_CUDA, LS_ERR_INVALID_ARG, LS_ERR_MISALIGNED,  # noqa: F401
+                   LS_ERR_UNSUPPORTED, LS_ERR_WORKSPACE, LS_F16, LS_F32, LS_OK, LsError,
+                   ls_layernorm_bw_dgamma_dbeta, ls_layernorm_bw_dgamma_dbeta_workspace_size,
+                   ls_layernorm_bw_dinp, ls_layernorm_fw, ls_softmax_bw, ls_softmax_fw, load,
+                   status_string)
+
+__all__ = [
+    "softmax_fw", "softmax_bw", "layernorm_fw", "layernorm_bw_dinp",
+    "layernorm_bw_dgamma_dbeta", "dgamma_dbeta_workspace", "LsError", "load",
+    "ls_softmax_fw", "ls_softmax_bw", "ls_layernorm_fw", "ls_layernorm_bw_dinp",
+    "ls_layernorm_bw_dgamma_dbeta", "ls_layernorm_bw_dgamma_dbeta_workspace_size",
+]
+
+
+def _torch():
+    import torch
+    return torch
+
+
+def ls_dtype(t) -> int:
+    torch = _torch()
+    m = {torch.float32: LS_F32, torch.float16: LS_F16, torch.bfloat16: LS_BF16}
+    if t.dtype not in m:
+        raise TypeError(f"unsupported storage dtype {t.dtype} (float32, float16, bfloat16)")
+    return m[t.dtype]
+
+
+def _stream(t) -> int:
+    torch = _torch()
+    return torch.cuda.current_stream(t.device).cuda_stream
+
+
+def _dev(*ts):
+    for t in ts:
+        if t is None:
+            continue
+        if not t.is_cuda:
+            raise ValueError("tensors must live on a CUDA device (there is no CPU path)")
+        if not t.is_contiguous():
+            raise ValueError("tensors must be contiguous")
+
+
+def _ptr(t) -> int:
+    return 0 if t is None else t.data_ptr()
+
+
+def _ok(status: int, where: str):
+    if status != LS_OK:
+        raise LsError(status, where)
+
+
+def softmax_fw(scores, mask=None, causal: bool = False, out=None):
+    """Softmax over the last axis of scores [B,H,Tq,Tk] plus an additive mask
+    [B,Tk] (broadcast over heads and queries), future keys j > i masked when
+    ``causal``.  ``out`` may be ``scores`` itself (in place)."""
+    torch = _torch()
+    if scores.dim() != 4:
+        raise ValueError("scores must be [B, H, Tq, Tk]")
+    B, H, Tq, Tk = scores.shape
+    if mask is not None and (tuple(mask.shape) != (B, Tk) or mask.dtype != scores.dtype):
+        raise ValueError("mask must be [B, Tk] with the scores' dtype")
+    out = torch.empty_like(scores) if out is None else out
+    _dev(scores, mask, out)
+    _ok(ls_softmax_fw(_ptr(out), _ptr(scores), _ptr(mask), B, H, Tq, Tk, causal,
+                      ls_dtype(scores), _stream(scores)), "ls_softmax_fw")
+    return out
+
+
+def softmax_bw(dout, out_fw, dinp=None):
+    """Gradient of the softmax input from the output gradient ``dout`` and the
+    forward output ``out_fw`` (both [B,H,Tq,Tk]).  ``dinp`` may be ``dout``."""
+    torch = _torch()
+    if dout.dim() != 4 or dout.shape != out_fw.shape or dout.dtype != out_fw.dtype:
+        raise ValueError("dout and out_fw must be [B, H, Tq, Tk] of one dtype")
+    B, H, Tq, Tk = dout.shape
+    dinp = torch.empty_like(dout) if dinp is None else dinp
+    _dev(dout, out_fw, dinp)
+    _ok(ls_softmax_bw(_ptr(dinp), _ptr(dout), _ptr(out_fw), B, H, Tq, Tk, ls_dtype(dout),
+                      _stream(dout)), "ls_softmax_bw")
+    return dinp
+
+
+def layernorm_fw(x, gamma, beta, eps: float = 1e-8, y=None, mean=None, rstd=None):
+    """LayerNorm of x [rows, hidden]; returns (y, mean, rstd), the statistics fp32."""
+    torch = _torch()
+    if x.dim() != 2:
+        raise ValueError("x must be [rows, hidden]")
+    rows, hidden = x.shape
+    y = torch.empty_like(x) if y is None else y
+    mean = torch.empty(rows, device=x.device, dtype=torch.float32) if mean is None else mean
+    rstd = torch.empty(rows, device=x.device, dtype=torch.float32) if rstd is None else rstd
+    _dev(x, gamma, beta, y, mean, rstd)
+    _ok(ls_layernorm_fw(_ptr(y), _ptr(mean), _ptr(rstd), _ptr(x), _ptr(gamma), _ptr(beta),
+                        rows, hidden, float(eps), ls_dtype(x), _stream(x)), "ls_layernorm_fw")
+    return y, mean, rstd
+
+
+def layernorm_bw_dinp(dy, x, gamma, mean, rstd, dx=None):
+    """Input gradient of LayerNorm from dy, x and the saved fp32 mean / rstd."""
+    torch = _torch()
+    rows, hidden = x.shape
+    dx = torch.empty_like(x) if dx is None else dx
+    _dev(dy, x, gamma, mean, rstd, dx)
+    _ok(ls_layernorm_bw_dinp(_ptr(dx), _ptr(dy), _ptr(x), _ptr(gamma), _ptr(mean), _ptr(rstd),
+                             rows, hidden, ls_dtype(x), _stream(x)), "ls_layernorm_bw_dinp")
+    return dx
+
+
+def dgamma_dbeta_workspace(rows: int, hidden: int, device):
+    """A workspace tensor of the size ls_layernorm_bw_dgamma_dbeta needs."""
+    torch = _torch()
+    n = ls_layernorm_bw_dgamma_dbeta_workspace_size(rows, hidden)
+    return torch.empty(max(n, 16) // 4, device=device, dtype=torch.float32)
+
+
+def layernorm_bw_dgamma_dbeta(dy, x, mean, rstd, workspace=None, dgamma=None, dbeta=None):
+    """gamma / beta gradients (fp32 [hidden]) summed over all rows, in a fixed
+    order (bitwise reproducible)."""
+    torch = _torch()
+    rows, hidden = x.shape
+    if workspace is None:
+        workspace = dgamma_dbeta_workspace(rows, hidden, x.device)
+    dgamma = torch.empty(hidden, device=x.device, dtype=torch.float32) if dgamma is None else dgamma
+    dbeta = torch.empty(hidden, device=x.device, dtype=torch.float32) if dbeta is None else dbeta
+    _dev(dy, x, mean, rstd, workspace, dgamma, dbeta)
+    _ok(ls_layernorm_bw_dgamma_dbeta(_ptr(dgamma), _ptr(dbeta), _ptr(dy), _ptr(x), _ptr(mean),
+                                     _ptr(rstd), rows, hidden, _ptr(workspace),
+                                     workspace.numel() * workspace.element_size(), ls_dtype(x),
+                                     _stream(x)), "ls_layernorm_bw_dgamma_dbeta")
+    return dgamma, dbeta

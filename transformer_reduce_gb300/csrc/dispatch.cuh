@@ -1,0 +1,220 @@
+// dispatch.cuh -- launch-time choice of the compile-time row shape.
+//
+// As the L10 page ("Technique 2", slides 24-26) describes for LightSeq, the
+// number of threads per row (TPR) and of 16-byte chunks per thread (CPT) are
+// template parameters; the launcher picks the smallest instantiation whose
+// capacity covers the row.  The HW4 page's ITERATIONS buckets for the softmax
+// backward (row lengths 32 ... 2048) all land on register-resident buckets
+// here:  16-bit storage holds up to 2048 elements in one warp (32 threads x 8
+// chunks x 8 elements); longer rows use 2..32 warps per row.
+#pragma once
+
+#include "launch.h"
+#include "layernorm.cuh"
+#include "softmax.cuh"
+
+namespace lsr {
+
+// Buckets: threads per row up to a cap chosen so that the launch bounds
+// (TPR threads per block) leave enough registers for CPT chunks per thread
+// without spilling.  Longer rows take the looped path.
+constexpr int kSoftmaxMaxCpt = 8;    // chunks per thread, softmax buckets
+constexpr int kSoftmaxMaxTpr = 256;  // 16-bit: 16384 keys per row in registers
+constexpr int kLnMaxCpt = 4;         // chunks per thread, LayerNorm buckets
+constexpr int kLnMaxTpr = 512;       // 16-bit: 16384 features per row in registers
+constexpr int kLoopWarpRowMax = 2048;  // looped path: one warp per row up to here
+
+template <int TPR>
+constexpr int block_threads() { return TPR <= 32 ? 256 : TPR; }
+template <int TPR>
+constexpr int rows_per_block() { return TPR <= 32 ? 256 / TPR : 1; }
+
+inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+inline int next_pow2(int64_t v) {
+    int p = 1;
+    while (p < v) p <<= 1;
+    return p;
+}
+
+// Bucket for a row of nchunk 16-byte chunks; false if it needs the looped path.
+inline bool pick_bucket(int64_t nchunk, int maxcpt, int maxtpr, int *tpr, int *cpt) {
+    if (nchunk <= 32) {
+        *tpr = next_pow2(nchunk < 1 ? 1 : nchunk);
+        *cpt = 1;
+    } else if (nchunk <= 32 * maxcpt) {
+        *tpr = 32;
+        *cpt = (int)ceil_div(nchunk, 32);
+    } else {
+        int64_t t = next_pow2(ceil_div(nchunk, maxcpt));
+        if (t > maxtpr) return false;
+        *tpr = (int)t;
+        *cpt = maxcpt;
+    }
+    return true;
+}
+
+// Resident blocks per SM of one kernel instantiation (queried once).
+template <auto K>
+int occupancy_per_sm(int block) {
+    static const int occ = [block] {
+        int n = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, K, block, 0) != cudaSuccess || n < 1)
+            n = 1;
+        return n;
+    }();
+    return occ;
+}
+
+// Persistent launch: as many blocks as fit on the GPU at once (never more than
+// there is work for); the kernels loop over their row groups.
+template <auto K, typename... Args>
+cudaError_t launch_persistent(int block, int64_t work_blocks, cudaStream_t st, Args... args) {
+    const int64_t cap = (int64_t)device_sm_count() * occupancy_per_sm<K>(block);
+    const int64_t grid = work_blocks < cap ? (work_blocks < 1 ? 1 : work_blocks) : cap;
+    K<<<(unsigned)grid, block, 0, st>>>(args...);
+    return cudaGetLastError();
+}
+
+// ----------------------------------------------------------------------------
+// softmax
+// ----------------------------------------------------------------------------
+#define LSR_SOFTMAX_BUCKETS(X)                                                  \
+    X(1, 1) X(2, 1) X(4, 1) X(8, 1) X(16, 1) X(32, 1) X(32, 2) X(32, 3) X(32, 4) \
+    X(32, 5) X(32, 6) X(32, 7) X(32, 8) X(64, 8) X(128, 8) X(256, 8)
+#define LSR_LN_BUCKETS(X)                                                       \
+    X(1, 1) X(2, 1) X(4, 1) X(8, 1) X(16, 1) X(32, 1) X(32, 2) X(32, 3) X(32, 4) \
+    X(64, 4) X(128, 4) X(256, 4) X(512, 4)
+
+template <typename T>
+cudaError_t launch_softmax_fw(T *out, const T *inp, const T *mask, int64_t rows,
+                              int64_t rows_per_batch, int64_t Tq, int64_t Tk,
+                              int causal, bool vec, cudaStream_t st) {
+    constexpr int V = Traits<T>::kVec;
+    int tpr = 0, cpt = 0;
+    if (vec && pick_bucket(Tk / V, kSoftmaxMaxCpt, kSoftmaxMaxTpr, &tpr, &cpt)) {
+#define X(TPR_, CPT_)                                                                   \
+    if (tpr == TPR_ && cpt == CPT_)                                                     \
+        return launch_persistent<softmax_fw_vec<T, TPR_, CPT_>>(                        \
+            block_threads<TPR_>(), ceil_div(rows, rows_per_block<TPR_>()), st, out, inp, \
+            mask, rows, rows_per_batch, Tq, (int)Tk, causal);
+        LSR_SOFTMAX_BUCKETS(X)
+#undef X
+    }
+    if (Tk <= kLoopWarpRowMax)
+        return launch_persistent<softmax_fw_loop<T, 32>>(256, ceil_div(rows, 8), st, out, inp,
+                                                         mask, rows, rows_per_batch, Tq, Tk,
+                                                         causal);
+    return launch_persistent<softmax_fw_loop<T, 256>>(256, rows, st, out, inp, mask, rows,
+                                                      rows_per_batch, Tq, Tk, causal);
+}
+
+template <typename T>
+cudaError_t launch_softmax_bw(T *dinp, const T *dout, const T *y, int64_t rows,
+                              int64_t Tk, bool vec, cudaStream_t st) {
+    constexpr int V = Traits<T>::kVec;
+    int tpr = 0, cpt = 0;
+    if (vec && pick_bucket(Tk / V, kSoftmaxMaxCpt, kSoftmaxMaxTpr, &tpr, &cpt)) {
+#define X(TPR_, CPT_)                                                                   \
+    if (tpr == TPR_ && cpt == CPT_)                                                     \
+        return launch_persistent<softmax_bw_vec<T, TPR_, CPT_>>(                        \
+            block_threads<TPR_>(), ceil_div(rows, rows_per_block<TPR_>()), st, dinp, dout, \
+            y, rows, (int)Tk);
+        LSR_SOFTMAX_BUCKETS(X)
+#undef X
+    }
+    if (Tk <= kLoopWarpRowMax)
+        return launch_persistent<softmax_bw_loop<T, 32>>(256, ceil_div(rows, 8), st, dinp, dout,
+                                                         y, rows, Tk);
+    return launch_persistent<softmax_bw_loop<T, 256>>(256, rows, st, dinp, dout, y, rows, Tk);
+}
+
+// ----------------------------------------------------------------------------
+// LayerNorm
+// ----------------------------------------------------------------------------
+template <typename T>
+cudaError_t launch_ln_fw(T *y, float *mean, float *rstd, const T *x, const T *gamma,
+                         const T *beta, int64_t rows, int64_t N, float eps, bool vec,
+                         cudaStream_t st) {
+    constexpr int V = Traits<T>::kVec;
+    int tpr = 0, cpt = 0;
+    if (vec && pick_bucket(N / V, kLnMaxCpt, kLnMaxTpr, &tpr, &cpt)) {
+#define X(TPR_, CPT_)                                                                     \
+    if (tpr == TPR_ && cpt == CPT_)                                                       \
+        return launch_persistent<ln_fw_vec<T, TPR_, CPT_>>(                               \
+            block_threads<TPR_>(), ceil_div(rows, rows_per_block<TPR_>()), st, y, mean, rstd, \
+            x, gamma, beta, rows, (int)N, eps);
+        LSR_LN_BUCKETS(X)
+#undef X
+    }
+    if (N <= kLoopWarpRowMax)
+        return launch_persistent<ln_fw_loop<T, 32>>(256, ceil_div(rows, 8), st, y, mean, rstd, x,
+                                                    gamma, beta, rows, N, eps);
+    return launch_persistent<ln_fw_loop<T, 256>>(256, rows, st, y, mean, rstd, x, gamma, beta,
+                                                 rows, N, eps);
+}
+
+template <typename T>
+cudaError_t launch_ln_dinp(T *dx, const T *dy, const T *x, const T *gamma,
+                           const float *mean, const float *rstd, int64_t rows,
+                           int64_t N, bool vec, cudaStream_t st) {
+    constexpr int V = Traits<T>::kVec;
+    int tpr = 0, cpt = 0;
+    if (vec && pick_bucket(N / V, kLnMaxCpt, kLnMaxTpr, &tpr, &cpt)) {
+#define X(TPR_, CPT_)                                                                       \
+    if (tpr == TPR_ && cpt == CPT_)                                                         \
+        return launch_persistent<ln_dinp_vec<T, TPR_, CPT_>>(                               \
+            block_threads<TPR_>(), ceil_div(rows, rows_per_block<TPR_>()), st, dx, dy, x, gamma, \
+            mean, rstd, rows, (int)N);
+        LSR_LN_BUCKETS(X)
+#undef X
+    }
+    if (N <= kLoopWarpRowMax)
+        return launch_persistent<ln_dinp_loop<T, 32>>(256, ceil_div(rows, 8), st, dx, dy, x,
+                                                      gamma, mean, rstd, rows, N);
+    return launch_persistent<ln_dinp_loop<T, 256>>(256, rows, st, dx, dy, x, gamma, mean, rstd,
+                                                   rows, N);
+}
+
+template <typename T>
+cudaError_t launch_ln_dgdb(float *dgamma, float *dbeta, const T *dy, const T *x,
+                           const float *mean, const float *rstd, int64_t rows,
+                           int64_t N, float *part, bool vec, cudaStream_t st) {
+    const int64_t rpc = dgdb_rows_per_chunk(rows, N);
+    const int64_t nchunks = dgdb_num_chunks(rows, N);
+    if (nchunks > 0) {
+        if (nchunks > 65535) return cudaErrorInvalidConfiguration;  // not reachable (rpc grows)
+        if (vec) {
+            constexpr int V = Traits<T>::kVec;
+            dim3 grid((unsigned)ceil_div(N, 32 * V), (unsigned)nchunks);
+            ln_dgdb_partial<T, V><<<grid, kDgdbWarps * 32, 0, st>>>(part, dy, x, mean, rstd,
+                                                                     rows, N, rpc);
+        } else {
+            dim3 grid((unsigned)ceil_div(N, 32), (unsigned)nchunks);
+            ln_dgdb_partial<T, 1><<<grid, kDgdbWarps * 32, 0, st>>>(part, dy, x, mean, rstd,
+                                                                     rows, N, rpc);
+        }
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    ln_dgdb_final<<<(unsigned)ceil_div(N, kFinalCols), kFinalCols * kFinalLanes, 0, st>>>(
+        dgamma, dbeta, part, nchunks, N);
+    return cudaGetLastError();
+}
+
+#define LSR_INSTANTIATE(T)                                                                      \
+    template cudaError_t launch_softmax_fw<T>(T *, const T *, const T *, int64_t, int64_t,     \
+                                              int64_t, int64_t, int, bool, cudaStream_t);      \
+    template cudaError_t launch_softmax_bw<T>(T *, const T *, const T *, int64_t, int64_t,     \
+                                              bool, cudaStream_t);                             \
+    template cudaError_t launch_ln_fw<T>(T *, float *, float *, const T *, const T *,          \
+                                         const T *, int64_t, int64_t, float, bool,             \
+                                         cudaStream_t);                                        \
+    template cudaError_t launch_ln_dinp<T>(T *, const T *, const T *, const T *,               \
+                                           const float *, const float *, int64_t, int64_t,     \
+                                           bool, cudaStream_t);                                \
+    template cudaError_t launch_ln_dgdb<T>(float *, float *, const T *, const T *,             \
+                                           const float *, const float *, int64_t, int64_t,     \
+                                           float *, bool, cudaStream_t);
+
+}  // namespace lsr

@@ -1,0 +1,42 @@
+// launch.h -- internal C++ launchers behind the C ABI (one instantiation per
+// storage dtype, compiled in its own translation unit).  Arguments have been
+// validated by the ABI layer; `vec` says whether every tensor of the call is
+// 16-byte aligned with a row length in bytes that is a multiple of 16.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace lsr {
+
+// Rows per partial-sum chunk of the gamma/beta reduction, and the chunk count.
+// Chosen so that column tiles x chunks gives roughly 512 blocks; depends only
+// on (rows, hidden), never on the GPU, so the summation order is fixed.
+int64_t dgdb_rows_per_chunk(int64_t rows, int64_t hidden);
+int64_t dgdb_num_chunks(int64_t rows, int64_t hidden);
+
+// Number of SMs of the current device (cached per device).
+int device_sm_count();
+
+template <typename T>
+cudaError_t launch_softmax_fw(T *out, const T *inp, const T *mask, int64_t rows,
+                              int64_t rows_per_batch, int64_t Tq, int64_t Tk,
+                              int causal, bool vec, cudaStream_t st);
+template <typename T>
+cudaError_t launch_softmax_bw(T *dinp, const T *dout, const T *y, int64_t rows,
+                              int64_t Tk, bool vec, cudaStream_t st);
+template <typename T>
+cudaError_t launch_ln_fw(T *y, float *mean, float *rstd, const T *x, const T *gamma,
+                         const T *beta, int64_t rows, int64_t N, float eps, bool vec,
+                         cudaStream_t st);
+template <typename T>
+cudaError_t launch_ln_dinp(T *dx, const T *dy, const T *x, const T *gamma,
+                           const float *mean, const float *rstd, int64_t rows,
+                           int64_t N, bool vec, cudaStream_t st);
+template <typename T>
+cudaError_t launch_ln_dgdb(float *dgamma, float *dbeta, const T *dy, const T *x,
+                           const float *mean, const float *rstd, int64_t rows,
+                           int64_t N, float *part, bool vec, cudaStream_t st);
+
+}  // namespace lsr

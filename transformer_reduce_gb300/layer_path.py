@@ -1,0 +1,193 @@
+"""One pass of the reduce hot path of a Transformer layer, through the C ABI.
+
+A pre-LayerNorm encoder layer touches the five kernels in this order on one
+stream (forward, then backward in reverse):
+
+    LN1 fw -> softmax fw -> LN2 fw -> LN2 bw (dinp, dgamma/dbeta)
+           -> softmax bw -> LN1 bw (dinp, dgamma/dbeta)
+
+``LayerReducePath`` owns the device buffers of one such pass (inputs drawn by
+``workloads``, outputs, the dgamma/dbeta workspaces) and issues the calls.
+Every call goes through ``_lib`` (raw pointers, the caller's stream); torch is
+used only to hold device and pinned host memory and to copy between them.
+"""
+from __future__ import annotations
+
+import dataclasses
+
+import torch
+
+from . import _lib, traffic, workloads
+
+_DT = {"f32": _lib.LS_F32, "f16": _lib.LS_F16, "bf16": _lib.LS_BF16}
+
+
+def _ok(status, where):
+    if status != _lib.LS_OK:
+        raise _lib.LsError(status, where)
+
+
+@dataclasses.dataclass
+class _LnBuffers:
+    case: workloads.LayerNormCase
+    x: torch.Tensor
+    gamma: torch.Tensor
+    beta: torch.Tensor
+    dy: torch.Tensor
+    y: torch.Tensor
+    mean: torch.Tensor
+    rstd: torch.Tensor
+    dx: torch.Tensor
+    dgamma: torch.Tensor
+    dbeta: torch.Tensor
+    ws: torch.Tensor
+
+
+class LayerReducePath:
+    def __init__(self, softmax_case: workloads.SoftmaxCase, ln_cases, device="cuda"):
+        self.device = torch.device(device)
+        self.sm = softmax_case
+        si = workloads.softmax_inputs(softmax_case, device=self.device)
+        self.lengths = si["lengths"]
+        self.scores, self.mask, self.dprobs = si["scores"], si["mask"], si["dout"]
+        self.probs = torch.empty_like(self.scores)
+        self.dscores = torch.empty_like(self.scores)
+        self.ln = []
+        for case in ln_cases:
+            li = workloads.layernorm_inputs(case, device=self.device)
+            n = _lib.ls_layernorm_bw_dgamma_dbeta_workspace_size(case.rows, case.hidden)
+            f32 = dict(device=self.device, dtype=torch.float32)
+            self.ln.append(_LnBuffers(
+                case=case, x=li["x"], gamma=li["gamma"], beta=li["beta"], dy=li["dy"],
+                y=torch.empty_like(li["x"]), mean=torch.empty(case.rows, **f32),
+                rstd=torch.empty(case.rows, **f32), dx=torch.empty_like(li["x"]),
+                dgamma=torch.empty(case.hidden, **f32), dbeta=torch.empty(case.hidden, **f32),
+                ws=torch.empty(max(n, 16) // 4, **f32)))
+        self._host = None
+
+    # ---- the hot path ------------------------------------------------------
+    def _ln_fw(self, b: _LnBuffers, st):
+        c = b.case
+        _ok(_lib.ls_layernorm_fw(b.y.data_ptr(), b.mean.data_ptr(), b.rstd.data_ptr(),
+                                 b.x.data_ptr(), b.gamma.data_ptr(), b.beta.data_ptr(),
+                                 c.rows, c.hidden, c.eps, _DT[c.dtype], st), "ls_layernorm_fw")
+
+    def _ln_dinp(self, b: _LnBuffers, st):
+        c = b.case
+        _ok(_lib.ls_layernorm_bw_dinp(b.dx.data_ptr(), b.dy.data_ptr(), b.x.data_ptr(),
+                                      b.gamma.data_ptr(), b.mean.data_ptr(), b.rstd.data_ptr(),
+                                      c.rows, c.hidden, _DT[c.dtype], st), "ls_layernorm_bw_dinp")
+
+    def _ln_dgdb(self, b: _LnBuffers, st):
+        c = b.case
+        _ok(_lib.ls_layernorm_bw_dgamma_dbeta(
+            b.dgamma.data_ptr(), b.dbeta.data_ptr(), b.dy.data_ptr(), b.x.data_ptr(),
+            b.mean.data_ptr(), b.rstd.data_ptr(), c.rows, c.hidden, b.ws.data_ptr(),
+            b.ws.numel() * 4, _DT[c.dtype], st), "ls_layernorm_bw_dgamma_dbeta")
+
+    def _softmax_fw(self, st):
+        s = self.sm
+        _ok(_lib.ls_softmax_fw(self.probs.data_ptr(), self.scores.data_ptr(),
+                               0 if self.mask is None else self.mask.data_ptr(),
+                               s.B, s.H, s.T, s.T, s.causal, _DT[s.dtype], st), "ls_softmax_fw")
+
+    def _softmax_bw(self, st):
+        s = self.sm
+        _ok(_lib.ls_softmax_bw(self.dscores.data_ptr(), self.dprobs.data_ptr(),
+                               self.probs.data_ptr(), s.B, s.H, s.T, s.T, _DT[s.dtype], st),
+            "ls_softmax_bw")
+
+    def sequence(self):
+        """The (name, call(stream_handle)) list of one pass, in stream order."""
+        ln1 = self.ln[0]
+        ln2 = self.ln[1] if len(self.ln) > 1 else None
+        seq = [("ln_fw", lambda st: self._ln_fw(ln1, st)),
+               ("softmax_fw", self._softmax_fw)]
+        if ln2 is not None:
+            seq += [("ln_fw", lambda st: self._ln_fw(ln2, st)),
+                    ("ln_dinp", lambda st: self._ln_dinp(ln2, st)),
+                    ("ln_dgdb", lambda st: self._ln_dgdb(ln2, st))]
+        seq += [("softmax_bw", self._softmax_bw),
+                ("ln_dinp", lambda st: self._ln_dinp(ln1, st)),
+                ("ln_dgdb", lambda st: self._ln_dgdb(ln1, st))]
+        return seq
+
+    def run(self, stream=None, timers=None):
+        """Enqueue one pass on `stream` (default: torch's current stream).
+        timers: optional dict name -> list; a (start, end) CUDA event pair
+        recorded on the same stream is appended around each call."""
+        stream = stream or torch.cuda.current_stream(self.device)
+        st = stream.cuda_stream
+        for name, call in self.sequence():
+            if timers is None:
+                call(st)
+                continue
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            call(st)
+            e1.record(stream)
+            timers.setdefault(name, []).append((e0, e1))
+
+    # ---- accounting ----------------------------------------------------------
+    def kernel_bytes(self) -> dict:
+        """Algorithmic bytes of each call of one pass (name -> list of bytes)."""
+        s = self.sm
+        out = {}
+        for name, _ in self.sequence():
+            out.setdefault(name, [])
+        out["softmax_fw"].append(traffic.softmax_fw_bytes(s.B, s.H, s.T, self.lengths, s.causal,
+                                                          s.dtype, self.mask is not None))
+        out["softmax_bw"].append(traffic.softmax_bw_bytes(s.B, s.H, s.T, s.dtype))
+        for b in self.ln:
+            c = b.case
+            out["ln_fw"].append(traffic.layernorm_fw_bytes(c.rows, c.hidden, c.dtype))
+            out["ln_dinp"].append(traffic.layernorm_dinp_bytes(c.rows, c.hidden, c.dtype))
+            out["ln_dgdb"].append(traffic.layernorm_dgdb_bytes(c.rows, c.hidden, c.dtype))
+        return out
+
+    def step_bytes(self) -> int:
+        return sum(sum(v) for v in self.kernel_bytes().values())
+
+    def rows(self) -> dict:
+        return {"softmax_rows": 2 * self.sm.rows,  # forward and backward
+                "layernorm_rows": sum(3 * b.case.rows for b in self.ln)}
+
+    # ---- end-to-end copies -----------------------------------------------------
+    def _inputs(self):
+        t = [self.scores, self.dprobs] + ([self.mask] if self.mask is not None else [])
+        for b in self.ln:
+            t += [b.x, b.gamma, b.beta, b.dy]
+        return t
+
+    def _outputs(self):
+        t = [self.probs, self.dscores]
+        for b in self.ln:
+            t += [b.y, b.mean, b.rstd, b.dx, b.dgamma, b.dbeta]
+        return t
+
+    def host_buffers(self):
+        """Pinned host copies of every input and output of a pass."""
+        if self._host is None:
+            self._host = ([x.cpu().pin_memory() for x in self._inputs()],
+                          [torch.empty(x.shape, dtype=x.dtype, pin_memory=True)
+                           for x in self._outputs()])
+        return self._host
+
+    def h2d_bytes(self) -> int:
+        return sum(x.numel() * x.element_size() for x in self._inputs())
+
+    def d2h_bytes(self) -> int:
+        return sum(x.numel() * x.element_size() for x in self._outputs())
+
+    def upload(self, stream):
+        hin, _ = self.host_buffers()
+        with torch.cuda.stream(stream):
+            for d, h in zip(self._inputs(), hin):
+                d.copy_(h, non_blocking=True)
+
+    def download(self, stream):
+        _, hout = self.host_buffers()
+        with torch.cuda.stream(stream):
+            for h, d in zip(hout, self._outputs()):
+                h.copy_(d, non_blocking=True)
