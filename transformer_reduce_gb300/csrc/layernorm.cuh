@@ -133,7 +133,9 @@ ln_dinp_vec(T *dx, const T *dy, const T *x, const T *gamma, const float *mean,
                 Tr::unpack(ld_cached16(gamma + c * V), gv);
 #pragma unroll
                 for (int e = 0; e < V; ++e) {
-                    g[k][e] *= gv[e];
+                    // rounded product (never fused into a later add), so that
+                    // S1 sums exactly the g the epilogue uses
+                    g[k][e] = __fmul_rn(g[k][e], gv[e]);
                     xh[k][e] = (xh[k][e] - mu) * rs;
                     s1 += g[k][e];
                     s2 = fmaf(g[k][e], xh[k][e], s2);
@@ -224,7 +226,8 @@ ln_dinp_loop(T *dx, const T *dy, const T *x, const T *gamma, const float *mean,
         float s1 = 0.f, s2 = 0.f;
         if (valid)
             for (int64_t j = lane; j < N; j += TPR) {
-                const float g = Tr::load1_cached(gamma + j) * Tr::load1(dy + off + j);
+                // rounded product (never fused), identical in both passes
+                const float g = __fmul_rn(Tr::load1_cached(gamma + j), Tr::load1(dy + off + j));
                 const float xh = (Tr::load1(x + off + j) - mu) * rs;
                 s1 += g;
                 s2 = fmaf(g, xh, s2);
@@ -233,7 +236,7 @@ ln_dinp_loop(T *dx, const T *dy, const T *x, const T *gamma, const float *mean,
         const float a = s1 * invN, b = s2 * invN;
         if (valid)
             for (int64_t j = lane; j < N; j += TPR) {
-                const float g = Tr::load1_cached(gamma + j) * Tr::load1(dy + off + j);
+                const float g = __fmul_rn(Tr::load1_cached(gamma + j), Tr::load1(dy + off + j));
                 const float xh = (Tr::load1(x + off + j) - mu) * rs;
                 Tr::store1(dx + off + j, rs * (g - a - xh * b));
             }
