@@ -179,6 +179,45 @@ ls_status ls_layernorm_bw_dgamma_dbeta(float *dgamma, float *dbeta,
                                        void *workspace, size_t workspace_bytes,
                                        ls_dtype dt, void *stream);
 
+/*
+ * Size of the device array that ls_layernorm_bw_dgamma_dbeta_noalloc uses as
+ * scratch (4 MiB).  It covers, for example, [16384, 8192] and [16384, 1024].
+ */
+#define LS_DGDB_NOALLOC_SCRATCH_BYTES ((size_t)4 << 20)
+
+/*
+ * LayerNorm gamma/beta gradients without any allocation.  The pages have no
+ * counterpart to this entry point; it exists for callers that cannot hand the
+ * library a workspace -- code that receives only tensor pointers and a stream
+ * from a host program (a plugin, or C code with no access to the host's
+ * allocator), or code that may not call cudaMalloc at that moment because
+ * cudaMalloc can synchronise the device or break the host's memory budget.
+ *
+ * Computes exactly what ls_layernorm_bw_dgamma_dbeta computes (same kernels,
+ * same fixed summation order, bitwise the same result), but keeps the partial
+ * sums in a fixed device array of LS_DGDB_NOALLOC_SCRATCH_BYTES compiled into
+ * the library, which every GPU that loads the library holds until the process
+ * exits.  It calls no cudaMalloc, cudaFree or other allocating routine.
+ *
+ *   Arguments as for ls_layernorm_bw_dgamma_dbeta, without the workspace.
+ *   Problems whose partial sums need more than LS_DGDB_NOALLOC_SCRATCH_BYTES
+ *   (ls_layernorm_bw_dgamma_dbeta_workspace_size(rows, hidden) larger than
+ *   that) are refused with LS_ERR_UNSUPPORTED before anything is launched.
+ *
+ * The first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current and caches it; make that
+ * first call before any stream capture.  All calls on a device share the one
+ * array: calls that may overlap on the GPU (different streams without
+ * ordering between them) race on it and must not be issued that way.  The
+ * array keeps the last call's partial sums; each call overwrites every
+ * partial it reads, so nothing needs to be cleared between calls.
+ */
+ls_status ls_layernorm_bw_dgamma_dbeta_noalloc(float *dgamma, float *dbeta,
+                                               const void *dy, const void *x,
+                                               const float *mean, const float *rstd,
+                                               int64_t rows, int64_t hidden,
+                                               ls_dtype dt, void *stream);
+
 /* Static, human-readable name of a status code (never NULL). */
 const char *ls_status_string(ls_status s);
 

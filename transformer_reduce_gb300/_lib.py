@@ -31,6 +31,8 @@ SIGNATURES = {
     "ls_layernorm_bw_dgamma_dbeta_workspace_size": ([_I64, _I64], _SZ),
     "ls_layernorm_bw_dgamma_dbeta": ([_VP, _VP, _VP, _VP, _VP, _VP, _I64, _I64, _VP, _SZ, _INT, _VP],
                                      _INT),
+    "ls_layernorm_bw_dgamma_dbeta_noalloc": ([_VP, _VP, _VP, _VP, _VP, _VP, _I64, _I64, _INT, _VP],
+                                             _INT),
     "ls_status_string": ([_INT], ctypes.c_char_p),
 }
 
@@ -91,3 +93,12 @@ def ls_layernorm_bw_dgamma_dbeta(dgamma, dbeta, dy, x, mean, rstd, rows, hidden,
                                  workspace_bytes, dt, stream=0) -> int:
     return load().ls_layernorm_bw_dgamma_dbeta(dgamma, dbeta, dy, x, mean, rstd, rows, hidden,
                                                workspace, workspace_bytes, dt, stream)
+
+
+def ls_layernorm_bw_dgamma_dbeta_noalloc(dgamma, dbeta, dy, x, mean, rstd, rows, hidden, dt,
+                                         stream=0) -> int:
+    """The gamma/beta gradient for callers that cannot allocate a workspace:
+    the library's own fixed device array holds the partial sums (see the
+    header for its size limit and the rule that overlapping calls race)."""
+    return load().ls_layernorm_bw_dgamma_dbeta_noalloc(dgamma, dbeta, dy, x, mean, rstd, rows,
+                                                       hidden, dt, stream)
