@@ -18,7 +18,7 @@ namespace lsr {
 int64_t dgdb_rows_per_chunk(int64_t rows, int64_t hidden) {
     if (rows <= 0 || hidden <= 0) return 1;
     const int64_t tiles = (hidden + 255) / 256;
-    int64_t target = rows * tiles / 512;
+    int64_t target = rows * tiles / 1024;
     int64_t rpc = 16;
     while (rpc < 256 && rpc * 2 <= target) rpc *= 2;
     while ((rows + rpc - 1) / rpc > 65535) rpc *= 2;

@@ -5,21 +5,27 @@
 // template parameters; the launcher picks the smallest instantiation whose
 // capacity covers the row.  The HW4 page's ITERATIONS buckets for the softmax
 // backward (row lengths 32 ... 2048) all land on register-resident buckets
-// here:  16-bit storage holds up to 2048 elements in one warp (32 threads x 8
-// chunks x 8 elements); longer rows use 2..32 warps per row.
+// here: 16-bit storage holds up to 2048 elements in one warp for the backward
+// (32 threads x 8 chunks x 8 elements) and 1024 for the pipelined forward
+// (which keeps two rows in registers); longer rows use several warps per row,
+// up to 16384 elements, and the looped path beyond.
 #pragma once
 
 #include "launch.h"
 #include "layernorm.cuh"
 #include "softmax.cuh"
 
+#include <atomic>
+
 namespace lsr {
 
 // Buckets: threads per row up to a cap chosen so that the launch bounds
 // (TPR threads per block) leave enough registers for CPT chunks per thread
 // without spilling.  Longer rows take the looped path.
-constexpr int kSoftmaxMaxCpt = 8;    // chunks per thread, softmax buckets
-constexpr int kSoftmaxMaxTpr = 256;  // 16-bit: 16384 keys per row in registers
+constexpr int kSoftmaxFwMaxCpt = 4;  // chunks per thread, softmax forward buckets
+constexpr int kSoftmaxFwMaxTpr = 512;  // 16-bit: 16384 keys per row in registers
+constexpr int kSoftmaxBwMaxCpt = 8;  // chunks per thread, softmax backward buckets
+constexpr int kSoftmaxBwMaxTpr = 256;  // 16-bit: 16384 keys per row in registers
 constexpr int kLnMaxCpt = 4;         // chunks per thread, LayerNorm buckets
 constexpr int kLnMaxTpr = 512;       // 16-bit: 16384 features per row in registers
 constexpr int kLoopWarpRowMax = 2048;  // looped path: one warp per row up to here
@@ -54,12 +60,24 @@ inline bool pick_bucket(int64_t nchunk, int maxcpt, int maxtpr, int *tpr, int *c
     return true;
 }
 
-// Resident blocks per SM of one kernel instantiation (queried once).
+constexpr int kMaxDevices = 64;
+
+// Resident blocks per SM of one kernel instantiation with `smem` bytes of
+// dynamic shared memory (queried once; the opt-in above 48 KB is set once per
+// device before the first launch there).
 template <auto K>
-int occupancy_per_sm(int block) {
-    static const int occ = [block] {
+int occupancy_per_sm(int block, size_t smem) {
+    static std::atomic<int> configured[kMaxDevices];
+    int dev = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess && dev >= 0 && dev < kMaxDevices &&
+        smem > 48 * 1024 && !configured[dev].load(std::memory_order_acquire)) {
+        cudaFuncSetAttribute(K, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        configured[dev].store(1, std::memory_order_release);
+    }
+    static const int occ = [block, smem] {
         int n = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, K, block, 0) != cudaSuccess || n < 1)
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, K, block, smem) != cudaSuccess ||
+            n < 1)
             n = 1;
         return n;
     }();
@@ -67,19 +85,28 @@ int occupancy_per_sm(int block) {
 }
 
 // Persistent launch: as many blocks as fit on the GPU at once (never more than
-// there is work for); the kernels loop over their row groups.
+// there is work for); the kernels loop over their rows.
 template <auto K, typename... Args>
-cudaError_t launch_persistent(int block, int64_t work_blocks, cudaStream_t st, Args... args) {
-    const int64_t cap = (int64_t)device_sm_count() * occupancy_per_sm<K>(block);
+cudaError_t launch_persistent(int block, size_t smem, int64_t work_blocks, cudaStream_t st,
+                              Args... args) {
+    const int64_t cap = (int64_t)device_sm_count() * occupancy_per_sm<K>(block, smem);
     const int64_t grid = work_blocks < cap ? (work_blocks < 1 ? 1 : work_blocks) : cap;
-    K<<<(unsigned)grid, block, 0, st>>>(args...);
+    K<<<(unsigned)grid, block, smem, st>>>(args...);
     return cudaGetLastError();
 }
+
+// Stages of the cp.async row pipelines (rows in flight per row group = S - 1).
+constexpr int kSoftmaxFwStages = 4;
+constexpr int kLnFwStages = 4;
+constexpr int kLnDinpStages = 3;
 
 // ----------------------------------------------------------------------------
 // softmax
 // ----------------------------------------------------------------------------
-#define LSR_SOFTMAX_BUCKETS(X)                                                  \
+#define LSR_SOFTMAX_FW_BUCKETS(X)                                               \
+    X(1, 1) X(2, 1) X(4, 1) X(8, 1) X(16, 1) X(32, 1) X(32, 2) X(32, 3) X(32, 4) \
+    X(64, 4) X(128, 4) X(256, 4) X(512, 4)
+#define LSR_SOFTMAX_BW_BUCKETS(X)                                               \
     X(1, 1) X(2, 1) X(4, 1) X(8, 1) X(16, 1) X(32, 1) X(32, 2) X(32, 3) X(32, 4) \
     X(32, 5) X(32, 6) X(32, 7) X(32, 8) X(64, 8) X(128, 8) X(256, 8)
 #define LSR_LN_BUCKETS(X)                                                       \
@@ -92,20 +119,21 @@ cudaError_t launch_softmax_fw(T *out, const T *inp, const T *mask, int64_t rows,
                               int causal, bool vec, cudaStream_t st) {
     constexpr int V = Traits<T>::kVec;
     int tpr = 0, cpt = 0;
-    if (vec && pick_bucket(Tk / V, kSoftmaxMaxCpt, kSoftmaxMaxTpr, &tpr, &cpt)) {
+    if (vec && pick_bucket(Tk / V, kSoftmaxFwMaxCpt, kSoftmaxFwMaxTpr, &tpr, &cpt)) {
 #define X(TPR_, CPT_)                                                                   \
     if (tpr == TPR_ && cpt == CPT_)                                                     \
-        return launch_persistent<softmax_fw_vec<T, TPR_, CPT_>>(                        \
-            block_threads<TPR_>(), ceil_div(rows, rows_per_block<TPR_>()), st, out, inp, \
-            mask, rows, rows_per_batch, Tq, (int)Tk, causal);
-        LSR_SOFTMAX_BUCKETS(X)
+        return launch_persistent<softmax_fw_vec<T, TPR_, CPT_, kSoftmaxFwStages>>(      \
+            block_threads<TPR_>(), softmax_fw_smem<TPR_, CPT_, kSoftmaxFwStages>(),        \
+            ceil_div(rows, rows_per_block<TPR_>()), st, out, inp, mask, rows,               \
+            rows_per_batch, Tq, (int)Tk, causal);
+        LSR_SOFTMAX_FW_BUCKETS(X)
 #undef X
     }
     if (Tk <= kLoopWarpRowMax)
-        return launch_persistent<softmax_fw_loop<T, 32>>(256, ceil_div(rows, 8), st, out, inp,
+        return launch_persistent<softmax_fw_loop<T, 32>>(256, 0, ceil_div(rows, 8), st, out, inp,
                                                          mask, rows, rows_per_batch, Tq, Tk,
                                                          causal);
-    return launch_persistent<softmax_fw_loop<T, 256>>(256, rows, st, out, inp, mask, rows,
+    return launch_persistent<softmax_fw_loop<T, 256>>(256, 0, rows, st, out, inp, mask, rows,
                                                       rows_per_batch, Tq, Tk, causal);
 }
 
@@ -114,19 +142,19 @@ cudaError_t launch_softmax_bw(T *dinp, const T *dout, const T *y, int64_t rows,
                               int64_t Tk, bool vec, cudaStream_t st) {
     constexpr int V = Traits<T>::kVec;
     int tpr = 0, cpt = 0;
-    if (vec && pick_bucket(Tk / V, kSoftmaxMaxCpt, kSoftmaxMaxTpr, &tpr, &cpt)) {
+    if (vec && pick_bucket(Tk / V, kSoftmaxBwMaxCpt, kSoftmaxBwMaxTpr, &tpr, &cpt)) {
 #define X(TPR_, CPT_)                                                                   \
     if (tpr == TPR_ && cpt == CPT_)                                                     \
         return launch_persistent<softmax_bw_vec<T, TPR_, CPT_>>(                        \
-            block_threads<TPR_>(), ceil_div(rows, rows_per_block<TPR_>()), st, dinp, dout, \
-            y, rows, (int)Tk);
-        LSR_SOFTMAX_BUCKETS(X)
+            block_threads<TPR_>(), 0, ceil_div(rows, rows_per_block<TPR_>()), st, dinp,     \
+            dout, y, rows, (int)Tk);
+        LSR_SOFTMAX_BW_BUCKETS(X)
 #undef X
     }
     if (Tk <= kLoopWarpRowMax)
-        return launch_persistent<softmax_bw_loop<T, 32>>(256, ceil_div(rows, 8), st, dinp, dout,
+        return launch_persistent<softmax_bw_loop<T, 32>>(256, 0, ceil_div(rows, 8), st, dinp, dout,
                                                          y, rows, Tk);
-    return launch_persistent<softmax_bw_loop<T, 256>>(256, rows, st, dinp, dout, y, rows, Tk);
+    return launch_persistent<softmax_bw_loop<T, 256>>(256, 0, rows, st, dinp, dout, y, rows, Tk);
 }
 
 // ----------------------------------------------------------------------------
@@ -141,16 +169,17 @@ cudaError_t launch_ln_fw(T *y, float *mean, float *rstd, const T *x, const T *ga
     if (vec && pick_bucket(N / V, kLnMaxCpt, kLnMaxTpr, &tpr, &cpt)) {
 #define X(TPR_, CPT_)                                                                     \
     if (tpr == TPR_ && cpt == CPT_)                                                       \
-        return launch_persistent<ln_fw_vec<T, TPR_, CPT_>>(                               \
-            block_threads<TPR_>(), ceil_div(rows, rows_per_block<TPR_>()), st, y, mean, rstd, \
-            x, gamma, beta, rows, (int)N, eps);
+        return launch_persistent<ln_fw_vec<T, TPR_, CPT_, kLnFwStages>>(                  \
+            block_threads<TPR_>(), ln_smem<TPR_, CPT_, kLnFwStages, 1, 1>(),                \
+            ceil_div(rows, rows_per_block<TPR_>()), st, y, mean, rstd, x, gamma, beta, rows,  \
+            (int)N, eps);
         LSR_LN_BUCKETS(X)
 #undef X
     }
     if (N <= kLoopWarpRowMax)
-        return launch_persistent<ln_fw_loop<T, 32>>(256, ceil_div(rows, 8), st, y, mean, rstd, x,
+        return launch_persistent<ln_fw_loop<T, 32>>(256, 0, ceil_div(rows, 8), st, y, mean, rstd, x,
                                                     gamma, beta, rows, N, eps);
-    return launch_persistent<ln_fw_loop<T, 256>>(256, rows, st, y, mean, rstd, x, gamma, beta,
+    return launch_persistent<ln_fw_loop<T, 256>>(256, 0, rows, st, y, mean, rstd, x, gamma, beta,
                                                  rows, N, eps);
 }
 
@@ -163,16 +192,17 @@ cudaError_t launch_ln_dinp(T *dx, const T *dy, const T *x, const T *gamma,
     if (vec && pick_bucket(N / V, kLnMaxCpt, kLnMaxTpr, &tpr, &cpt)) {
 #define X(TPR_, CPT_)                                                                       \
     if (tpr == TPR_ && cpt == CPT_)                                                         \
-        return launch_persistent<ln_dinp_vec<T, TPR_, CPT_>>(                               \
-            block_threads<TPR_>(), ceil_div(rows, rows_per_block<TPR_>()), st, dx, dy, x, gamma, \
-            mean, rstd, rows, (int)N);
+        return launch_persistent<ln_dinp_vec<T, TPR_, CPT_, kLnDinpStages>>(                \
+            block_threads<TPR_>(), ln_smem<TPR_, CPT_, kLnDinpStages, 2, 2>(),                \
+            ceil_div(rows, rows_per_block<TPR_>()), st, dx, dy, x, gamma, mean, rstd, rows,     \
+            (int)N);
         LSR_LN_BUCKETS(X)
 #undef X
     }
     if (N <= kLoopWarpRowMax)
-        return launch_persistent<ln_dinp_loop<T, 32>>(256, ceil_div(rows, 8), st, dx, dy, x,
+        return launch_persistent<ln_dinp_loop<T, 32>>(256, 0, ceil_div(rows, 8), st, dx, dy, x,
                                                       gamma, mean, rstd, rows, N);
-    return launch_persistent<ln_dinp_loop<T, 256>>(256, rows, st, dx, dy, x, gamma, mean, rstd,
+    return launch_persistent<ln_dinp_loop<T, 256>>(256, 0, rows, st, dx, dy, x, gamma, mean, rstd,
                                                    rows, N);
 }
 

@@ -11,7 +11,7 @@
 namespace lsr {
 
 // Rows per partial-sum chunk of the gamma/beta reduction, and the chunk count.
-// Chosen so that column tiles x chunks gives roughly 512 blocks; depends only
+// Chosen so that column tiles x chunks gives roughly 1024 blocks; depends only
 // on (rows, hidden), never on the GPU, so the summation order is fixed.
 int64_t dgdb_rows_per_chunk(int64_t rows, int64_t hidden);
 int64_t dgdb_num_chunks(int64_t rows, int64_t hidden);

@@ -24,136 +24,248 @@
 
 namespace lsr {
 
+// First element of a row from the 4 bytes copied at its start.
+template <typename T>
+__device__ __forceinline__ float first_elem(uint32_t w);
+template <>
+__device__ __forceinline__ float first_elem<float>(uint32_t w) { return __uint_as_float(w); }
+template <>
+__device__ __forceinline__ float first_elem<__half>(uint32_t w) {
+    return __half2float(__ushort_as_half((unsigned short)(w & 0xffffu)));
+}
+template <>
+__device__ __forceinline__ float first_elem<__nv_bfloat16>(uint32_t w) {
+    return __uint_as_float(w << 16);
+}
+
+// Shared memory of the staged LayerNorm kernels: S stages of A tensors x CPT
+// 16-byte chunks per thread, plus W words of per-row scalars per stage.
+template <int TPR, int CPT, int S, int A, int W>
+constexpr size_t ln_smem() {
+    return (size_t)S * (TPR <= 32 ? 256 : TPR) * (A * CPT * 16 + W * 4);
+}
+
 // ----------------------------------------------------------------------------
-// Forward, register resident.  The two statistics come from ONE fused
-// reduction of sum(x') and sum(x'^2) with x' = x - x0 (x0 = the row's first
-// element): var = mean(x'^2) - mean(x')^2 is the one-pass form, and the shift
-// removes its cancellation when |mean| >> std (it is exact for constant rows).
+// Forward.  The two statistics come from ONE fused reduction of sum(x') and
+// sum(x'^2) with x' = x - x0 (x0 = the row's first element): var =
+// mean(x'^2) - mean(x')^2 is the one-pass form, and the shift removes its
+// cancellation when |mean| >> std (it is exact for constant rows).
+//
+// Each row group owns a contiguous range of rows.  Rows are staged into
+// shared memory S-1 rows ahead with per-thread cp.async copies (each thread
+// reads back only its own chunks), so the loads of several rows are in
+// flight while one is reduced.  A thread's columns are the same for every
+// row: its gamma/beta chunks are loaded once.  Arithmetic is packed FP32x2.
 // ----------------------------------------------------------------------------
-template <typename T, int TPR, int CPT>
-__global__ void __launch_bounds__(TPR <= 32 ? 256 : TPR)
+template <typename T, int TPR, int CPT, int S>
+__global__ void __launch_bounds__(TPR <= 32 ? 256 : TPR, (row_kernel_min_blocks<TPR, CPT>()))
 ln_fw_vec(T *y, float *mean, float *rstd, const T *x, const T *gamma,
           const T *beta, int64_t rows, int N, float eps) {
     using Tr = Traits<T>;
     constexpr int V = Tr::kVec;
+    constexpr int H2 = V / 2;
     constexpr int BLOCK = TPR <= 32 ? 256 : TPR;
     constexpr int G = BLOCK / TPR;
+    extern __shared__ uint4 dsmem[];
+    uint4 *stage = dsmem;                                                  // [S][CPT][BLOCK]
+    uint32_t *x0b = reinterpret_cast<uint32_t *>(dsmem + S * CPT * BLOCK);  // [S][BLOCK]
     __shared__ float red[TPR > 32 ? 64 : 1];
 
-    const int lane = threadIdx.x % TPR;
-    const int grp = threadIdx.x / TPR;
+    const int tid = threadIdx.x;
+    const int lane = tid % TPR;
+    const int grp = tid / TPR;
     const int nchunk = N / V;
     const float invN = 1.f / (float)N;
+    const int64_t ngroups = (int64_t)gridDim.x * G;
+    const int64_t per = (rows + ngroups - 1) / ngroups;
+    const int64_t rbeg = ((int64_t)blockIdx.x * G + grp) * per;
+    const int64_t rend = rbeg + per < rows ? rbeg + per : rows;
+    const uint64_t pol = l2_evict_first_policy();
 
-    for (int64_t base = (int64_t)blockIdx.x * G; base < rows;
-         base += (int64_t)gridDim.x * G) {
-        const int64_t row = base + grp;
-        const bool valid = row < rows;
-        const T *xrow = x + row * (int64_t)N;
-        const float x0 = valid ? Tr::load1_cached(xrow) : 0.f;
-
-        float d[CPT][V];
-        float s1 = 0.f, s2 = 0.f;
+    uint4 gr[CPT], br[CPT];
 #pragma unroll
-        for (int k = 0; k < CPT; ++k) {
-            const int c = k * TPR + lane;
+    for (int k = 0; k < CPT; ++k) {
+        const int c = k * TPR + lane;
+        if (c < nchunk) {
+            gr[k] = ld_cached16(gamma + c * V);
+            br[k] = ld_cached16(beta + c * V);
+        }
+    }
+    int64_t inext = rbeg;
+    auto issue = [&](int s) {
+        if (inext < rend) {
+            const T *xrow = x + inext * (int64_t)N;
+#pragma unroll
+            for (int k = 0; k < CPT; ++k) {
+                const int c = k * TPR + lane;
+                if (c < nchunk) cp_async16(&stage[(s * CPT + k) * BLOCK + tid], xrow + c * V, pol);
+            }
+            cp_async4(&x0b[s * BLOCK + tid], xrow);
+        }
+        ++inext;
+        cp_async_commit();
+    };
+#pragma unroll
+    for (int s = 0; s < S - 1; ++s) issue(s);
+
+    int s_cur = 0, s_iss = S - 1;
+    for (int64_t k = 0; k < per; ++k) {
+        issue(s_iss);
+        s_iss = s_iss + 1 == S ? 0 : s_iss + 1;
+        cp_async_wait<S - 1>();
+
+        const int64_t row = rbeg + k;
+        const bool valid = row < rend;
+        const float x0 = valid ? first_elem<T>(x0b[s_cur * BLOCK + tid]) : 0.f;
+        float2 d[CPT][H2];
+        float2 s1 = f2(0.f), s2 = f2(0.f);
+#pragma unroll
+        for (int kk = 0; kk < CPT; ++kk) {
+            const int c = kk * TPR + lane;
             if (valid && c < nchunk) {
-                Tr::unpack(ld_stream16(xrow + c * V), d[k]);
+                unpack2<T>(stage[(s_cur * CPT + kk) * BLOCK + tid], d[kk]);
 #pragma unroll
-                for (int e = 0; e < V; ++e) {
-                    d[k][e] -= x0;
-                    s1 += d[k][e];
-                    s2 = fmaf(d[k][e], d[k][e], s2);
+                for (int h = 0; h < H2; ++h) {
+                    d[kk][h] = __fadd2_rn(d[kk][h], f2(-x0));
+                    s1 = __fadd2_rn(s1, d[kk][h]);
+                    s2 = __ffma2_rn(d[kk][h], d[kk][h], s2);
                 }
             }
         }
-        group_sum2<TPR>(s1, s2, red);
-        const float m1 = s1 * invN;
-        const float var = fmaxf(s2 * invN - m1 * m1, 0.f);
+        float a1 = s1.x + s1.y, a2 = s2.x + s2.y;
+        group_sum2<TPR>(a1, a2, red);
+        const float m1 = a1 * invN;
+        const float var = fmaxf(a2 * invN - m1 * m1, 0.f);
         const float rs = rsqrtf(var + eps);
 
         T *yrow = y + row * (int64_t)N;
 #pragma unroll
-        for (int k = 0; k < CPT; ++k) {
-            const int c = k * TPR + lane;
+        for (int kk = 0; kk < CPT; ++kk) {
+            const int c = kk * TPR + lane;
             if (valid && c < nchunk) {
-                float gv[V], bv[V], yv[V];
-                Tr::unpack(ld_cached16(gamma + c * V), gv);
-                Tr::unpack(ld_cached16(beta + c * V), bv);
+                float2 gv[H2], bv[H2], yv[H2];
+                unpack2<T>(gr[kk], gv);
+                unpack2<T>(br[kk], bv);
 #pragma unroll
-                for (int e = 0; e < V; ++e)
-                    yv[e] = fmaf((d[k][e] - m1) * rs, gv[e], bv[e]);
-                st_stream16(yrow + c * V, Tr::pack(yv));
+                for (int h = 0; h < H2; ++h) {
+                    const float2 t = __fmul2_rn(__fadd2_rn(d[kk][h], f2(-m1)), f2(rs));
+                    yv[h] = __ffma2_rn(t, gv[h], bv[h]);
+                }
+                st_stream16(yrow + c * V, pack2<T>(yv));
             }
         }
         if (valid && lane == 0) {
             mean[row] = x0 + m1;
             rstd[row] = rs;
         }
+        s_cur = s_cur + 1 == S ? 0 : s_cur + 1;
     }
 }
 
 // ----------------------------------------------------------------------------
-// Input gradient, register resident.  g = gamma * dy, xhat = (x - mean)*rstd;
-// S1 = sum g and S2 = sum g*xhat in one fused reduction; then
-// dx = rstd * (g - S1/N - xhat * S2/N).
+// Input gradient.  g = gamma * dy, xhat = (x - mean)*rstd; S1 = sum g and
+// S2 = sum g*xhat in one fused reduction; then dx = rstd*(g - S1/N - xhat*S2/N).
+// Same staging as the forward (dy, x and the row's mean / rstd per stage).
 // ----------------------------------------------------------------------------
-template <typename T, int TPR, int CPT>
-__global__ void __launch_bounds__(TPR <= 32 ? 256 : TPR)
+template <typename T, int TPR, int CPT, int S>
+__global__ void __launch_bounds__(TPR <= 32 ? 256 : TPR, (row_kernel_min_blocks<TPR, CPT>()))
 ln_dinp_vec(T *dx, const T *dy, const T *x, const T *gamma, const float *mean,
             const float *rstd, int64_t rows, int N) {
     using Tr = Traits<T>;
     constexpr int V = Tr::kVec;
+    constexpr int H2 = V / 2;
     constexpr int BLOCK = TPR <= 32 ? 256 : TPR;
     constexpr int G = BLOCK / TPR;
+    extern __shared__ uint4 dsmem[];
+    uint4 *stage = dsmem;                                                    // [S][2][CPT][BLOCK]
+    float *stat = reinterpret_cast<float *>(dsmem + S * 2 * CPT * BLOCK);    // [S][2][BLOCK]
     __shared__ float red[TPR > 32 ? 64 : 1];
 
-    const int lane = threadIdx.x % TPR;
-    const int grp = threadIdx.x / TPR;
+    const int tid = threadIdx.x;
+    const int lane = tid % TPR;
+    const int grp = tid / TPR;
     const int nchunk = N / V;
     const float invN = 1.f / (float)N;
+    const int64_t ngroups = (int64_t)gridDim.x * G;
+    const int64_t per = (rows + ngroups - 1) / ngroups;
+    const int64_t rbeg = ((int64_t)blockIdx.x * G + grp) * per;
+    const int64_t rend = rbeg + per < rows ? rbeg + per : rows;
+    const uint64_t pol = l2_evict_first_policy();
 
-    for (int64_t base = (int64_t)blockIdx.x * G; base < rows;
-         base += (int64_t)gridDim.x * G) {
-        const int64_t row = base + grp;
-        const bool valid = row < rows;
-        const int64_t off = row * (int64_t)N;
-        const float mu = valid ? __ldg(mean + row) : 0.f;
-        const float rs = valid ? __ldg(rstd + row) : 0.f;
-
-        float g[CPT][V], xh[CPT][V];
-        float s1 = 0.f, s2 = 0.f;
+    uint4 gr[CPT];
 #pragma unroll
-        for (int k = 0; k < CPT; ++k) {
-            const int c = k * TPR + lane;
+    for (int k = 0; k < CPT; ++k) {
+        const int c = k * TPR + lane;
+        if (c < nchunk) gr[k] = ld_cached16(gamma + c * V);
+    }
+    int64_t inext = rbeg;
+    auto issue = [&](int s) {
+        if (inext < rend) {
+            const int64_t off = inext * (int64_t)N;
+#pragma unroll
+            for (int k = 0; k < CPT; ++k) {
+                const int c = k * TPR + lane;
+                if (c < nchunk) {
+                    cp_async16(&stage[((s * 2 + 0) * CPT + k) * BLOCK + tid], dy + off + c * V, pol);
+                    cp_async16(&stage[((s * 2 + 1) * CPT + k) * BLOCK + tid], x + off + c * V, pol);
+                }
+            }
+            cp_async4(&stat[(s * 2 + 0) * BLOCK + tid], mean + inext);
+            cp_async4(&stat[(s * 2 + 1) * BLOCK + tid], rstd + inext);
+        }
+        ++inext;
+        cp_async_commit();
+    };
+#pragma unroll
+    for (int s = 0; s < S - 1; ++s) issue(s);
+
+    int s_cur = 0, s_iss = S - 1;
+    for (int64_t k = 0; k < per; ++k) {
+        issue(s_iss);
+        s_iss = s_iss + 1 == S ? 0 : s_iss + 1;
+        cp_async_wait<S - 1>();
+
+        const int64_t row = rbeg + k;
+        const bool valid = row < rend;
+        const float mu = valid ? stat[(s_cur * 2 + 0) * BLOCK + tid] : 0.f;
+        const float rs = valid ? stat[(s_cur * 2 + 1) * BLOCK + tid] : 0.f;
+        float2 g[CPT][H2], xh[CPT][H2];
+        float2 s1 = f2(0.f), s2 = f2(0.f);
+#pragma unroll
+        for (int kk = 0; kk < CPT; ++kk) {
+            const int c = kk * TPR + lane;
             if (valid && c < nchunk) {
-                float gv[V];
-                Tr::unpack(ld_stream16(dy + off + c * V), g[k]);
-                Tr::unpack(ld_stream16(x + off + c * V), xh[k]);
-                Tr::unpack(ld_cached16(gamma + c * V), gv);
+                float2 gv[H2];
+                unpack2<T>(stage[((s_cur * 2 + 0) * CPT + kk) * BLOCK + tid], g[kk]);
+                unpack2<T>(stage[((s_cur * 2 + 1) * CPT + kk) * BLOCK + tid], xh[kk]);
+                unpack2<T>(gr[kk], gv);
 #pragma unroll
-                for (int e = 0; e < V; ++e) {
+                for (int h = 0; h < H2; ++h) {
                     // rounded product (never fused into a later add), so that
                     // S1 sums exactly the g the epilogue uses
-                    g[k][e] = __fmul_rn(g[k][e], gv[e]);
-                    xh[k][e] = (xh[k][e] - mu) * rs;
-                    s1 += g[k][e];
-                    s2 = fmaf(g[k][e], xh[k][e], s2);
+                    g[kk][h] = __fmul2_rn(g[kk][h], gv[h]);
+                    xh[kk][h] = __fmul2_rn(__fadd2_rn(xh[kk][h], f2(-mu)), f2(rs));
+                    s1 = __fadd2_rn(s1, g[kk][h]);
+                    s2 = __ffma2_rn(g[kk][h], xh[kk][h], s2);
                 }
             }
         }
-        group_sum2<TPR>(s1, s2, red);
-        const float a = s1 * invN, b = s2 * invN;
+        float a1 = s1.x + s1.y, a2 = s2.x + s2.y;
+        group_sum2<TPR>(a1, a2, red);
+        const float2 na = f2(-a1 * invN), nb = f2(-a2 * invN);
+        const int64_t off = row * (int64_t)N;
 #pragma unroll
-        for (int k = 0; k < CPT; ++k) {
-            const int c = k * TPR + lane;
+        for (int kk = 0; kk < CPT; ++kk) {
+            const int c = kk * TPR + lane;
             if (valid && c < nchunk) {
-                float dv[V];
+                float2 ov[H2];
 #pragma unroll
-                for (int e = 0; e < V; ++e) dv[e] = rs * (g[k][e] - a - xh[k][e] * b);
-                st_stream16(dx + off + c * V, Tr::pack(dv));
+                for (int h = 0; h < H2; ++h)
+                    ov[h] = __fmul2_rn(f2(rs), __ffma2_rn(xh[kk][h], nb, __fadd2_rn(g[kk][h], na)));
+                st_stream16(dx + off + c * V, pack2<T>(ov));
             }
         }
+        s_cur = s_cur + 1 == S ? 0 : s_cur + 1;
     }
 }
 
@@ -255,7 +367,7 @@ ln_dinp_loop(T *dx, const T *dy, const T *x, const T *gamma, const float *mean,
 constexpr int kDgdbWarps = 8;
 
 template <typename T, int V>
-__global__ void __launch_bounds__(kDgdbWarps * 32)
+__global__ void __launch_bounds__(kDgdbWarps * 32, 4)
 ln_dgdb_partial(float *part, const T *dy, const T *x, const float *mean,
                 const float *rstd, int64_t rows, int64_t N, int64_t rows_per_chunk) {
     using Tr = Traits<T>;
@@ -278,27 +390,44 @@ ln_dgdb_partial(float *part, const T *dy, const T *x, const float *mean,
         int64_t r = r0 + w;
         // Four rows in flight per warp per iteration.
         for (; r + 3 * kDgdbWarps < r1; r += 4 * kDgdbWarps) {
-            float dv[4][V], xv[4][V], mu[4], rs[4];
+            float mu[4], rs[4];
+            if constexpr (V == 1) {
+                float dv[4], xv[4];
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int64_t rr = r + u * kDgdbWarps;
-                mu[u] = __ldg(mean + rr);
-                rs[u] = __ldg(rstd + rr);
-                if constexpr (V == 1) {
-                    dv[u][0] = Tr::load1(dy + rr * N + col0);
-                    xv[u][0] = Tr::load1(x + rr * N + col0);
-                } else {
-                    Tr::unpack(ld_stream16(dy + rr * N + col0), dv[u]);
-                    Tr::unpack(ld_stream16(x + rr * N + col0), xv[u]);
+                for (int u = 0; u < 4; ++u) {
+                    const int64_t rr = r + u * kDgdbWarps;
+                    mu[u] = __ldg(mean + rr);
+                    rs[u] = __ldg(rstd + rr);
+                    dv[u] = Tr::load1(dy + rr * N + col0);
+                    xv[u] = Tr::load1(x + rr * N + col0);
+                }
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    ag[0] = fmaf(dv[u], (xv[u] - mu[u]) * rs[u], ag[0]);
+                    ab[0] += dv[u];
+                }
+            } else {
+                uint4 rdy[4], rx[4];  // raw 16-byte chunks: 4 rows in flight
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int64_t rr = r + u * kDgdbWarps;
+                    mu[u] = __ldg(mean + rr);
+                    rs[u] = __ldg(rstd + rr);
+                    rdy[u] = ld_stream16(dy + rr * N + col0);
+                    rx[u] = ld_stream16(x + rr * N + col0);
+                }
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    float dv[V], xv[V];
+                    Tr::unpack(rdy[u], dv);
+                    Tr::unpack(rx[u], xv);
+#pragma unroll
+                    for (int e = 0; e < V; ++e) {
+                        ag[e] = fmaf(dv[e], (xv[e] - mu[u]) * rs[u], ag[e]);
+                        ab[e] += dv[e];
+                    }
                 }
             }
-#pragma unroll
-            for (int u = 0; u < 4; ++u)
-#pragma unroll
-                for (int e = 0; e < V; ++e) {
-                    ag[e] = fmaf(dv[u][e], (xv[u][e] - mu[u]) * rs[u], ag[e]);
-                    ab[e] += dv[u][e];
-                }
         }
         for (; r < r1; r += kDgdbWarps) {
             float dv[V], xv[V];
@@ -355,6 +484,7 @@ ln_dgdb_final(float *dgamma, float *dbeta, const float *part, int64_t nchunks, i
     const int64_t col = (int64_t)blockIdx.x * kFinalCols + tx;
     float a = 0.f, b = 0.f;
     if (col < N)
+#pragma unroll 8
         for (int64_t c = ty; c < nchunks; c += kFinalLanes) {
             a += __ldcs(part + (c * 2 + 0) * N + col);
             b += __ldcs(part + (c * 2 + 1) * N + col);

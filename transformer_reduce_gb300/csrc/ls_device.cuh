@@ -100,6 +100,86 @@ struct Traits<__nv_bfloat16> {
     }
 };
 
+// Two-element views of a 16-byte vector, for the packed FP32x2 arithmetic of
+// sm_100+ (__fadd2_rn / __fmul2_rn / __ffma2_rn: two FP32 lanes per
+// instruction, each rounded like its scalar counterpart).
+template <typename T>
+__device__ __forceinline__ void unpack2(const uint4 &u, float2 (&f)[Traits<T>::kVec / 2]);
+template <>
+__device__ __forceinline__ void unpack2<float>(const uint4 &u, float2 (&f)[2]) {
+    f[0] = make_float2(__uint_as_float(u.x), __uint_as_float(u.y));
+    f[1] = make_float2(__uint_as_float(u.z), __uint_as_float(u.w));
+}
+template <>
+__device__ __forceinline__ void unpack2<__half>(const uint4 &u, float2 (&f)[4]) {
+    f[0] = Traits<__half>::two(u.x);
+    f[1] = Traits<__half>::two(u.y);
+    f[2] = Traits<__half>::two(u.z);
+    f[3] = Traits<__half>::two(u.w);
+}
+// bf16 is the upper half of an fp32: widening is a shift / a mask.
+__device__ __forceinline__ float2 bf16x2_to_float2(uint32_t w) {
+    return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+}
+template <>
+__device__ __forceinline__ void unpack2<__nv_bfloat16>(const uint4 &u, float2 (&f)[4]) {
+    f[0] = bf16x2_to_float2(u.x);
+    f[1] = bf16x2_to_float2(u.y);
+    f[2] = bf16x2_to_float2(u.z);
+    f[3] = bf16x2_to_float2(u.w);
+}
+template <typename T>
+__device__ __forceinline__ uint4 pack2(const float2 (&f)[Traits<T>::kVec / 2]);
+template <>
+__device__ __forceinline__ uint4 pack2<float>(const float2 (&f)[2]) {
+    return make_uint4(__float_as_uint(f[0].x), __float_as_uint(f[0].y), __float_as_uint(f[1].x),
+                      __float_as_uint(f[1].y));
+}
+template <>
+__device__ __forceinline__ uint4 pack2<__half>(const float2 (&f)[4]) {
+    return make_uint4(Traits<__half>::word(f[0].x, f[0].y), Traits<__half>::word(f[1].x, f[1].y),
+                      Traits<__half>::word(f[2].x, f[2].y), Traits<__half>::word(f[3].x, f[3].y));
+}
+template <>
+__device__ __forceinline__ uint4 pack2<__nv_bfloat16>(const float2 (&f)[4]) {
+    using B = Traits<__nv_bfloat16>;
+    return make_uint4(B::word(f[0].x, f[0].y), B::word(f[1].x, f[1].y), B::word(f[2].x, f[2].y),
+                      B::word(f[3].x, f[3].y));
+}
+__device__ __forceinline__ float2 f2(float a) { return make_float2(a, a); }
+
+// ----------------------------------------------------------------------------
+// Asynchronous global -> shared copies (cp.async, sm_80+).  Each thread copies
+// its own 16-byte chunks into its own shared-memory slots and later reads only
+// those slots, so `cp.async.wait_group` (which waits for the calling thread's
+// own copies and always completes) is the only synchronisation needed: no
+// barrier, no flag, no spin loop.  The L2 policy marks the streamed data
+// evict-first, as the __ldcs loads do.
+// ----------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_addr(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+__device__ __forceinline__ void cp_async16(void *dst, const void *src, uint64_t pol) {
+    asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;"
+                 :: "r"(smem_addr(dst)), "l"(src), "l"(pol) : "memory");
+}
+__device__ __forceinline__ void cp_async4(void *dst, const void *src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" :: "r"(smem_addr(dst)), "l"(src)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" :: "n"(N) : "memory");
+}
+
 // Streaming 128-bit accesses for tensors touched once per call (evict-first),
 // read-only cached 128-bit loads for the small operands every row re-reads
 // (gamma, beta, the mask row).
@@ -111,6 +191,16 @@ __device__ __forceinline__ uint4 ld_cached16(const void *p) {
 }
 __device__ __forceinline__ void st_stream16(void *p, const uint4 &v) {
     __stcs(reinterpret_cast<uint4 *>(p), v);
+}
+
+// Minimum resident blocks per SM asked of ptxas for a pipelined row kernel
+// with TPR threads per row and CPT chunks per thread: 64 registers per thread
+// for 1-2 chunks (4 blocks of 256 threads), 128 for more chunks or multi-warp
+// rows (2048 / 16 = 128 resident threads per 16K registers ...), so that
+// enough rows stay in flight to keep HBM busy without spilling.
+template <int TPR, int CPT>
+constexpr int row_kernel_min_blocks() {
+    return TPR <= 32 ? (CPT <= 2 ? 4 : 2) : (512 / TPR > 0 ? 512 / TPR : 1);
 }
 
 // ----------------------------------------------------------------------------
@@ -218,5 +308,14 @@ __device__ __forceinline__ void group_ms_merge(float &m, float &s, float *smem) 
 }
 
 constexpr float kLog2e = 1.4426950408889634f;
+
+// 2^x with the hardware approximation (PTX ex2.approx.ftz.f32: relative error
+// about 2^-22; results below 2^-126 flush to 0, which is far below any
+// tolerance here).  Used where the argument is already scaled by log2(e).
+__device__ __forceinline__ float fast_exp2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
 
 }  // namespace lsr

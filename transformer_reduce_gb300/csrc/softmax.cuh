@@ -30,86 +30,215 @@ namespace lsr {
 
 // ----------------------------------------------------------------------------
 // Register-resident forward: one row per TPR threads, CPT chunks per thread.
+//
+// Each row group owns a contiguous range of rows (rows of one batch entry
+// share the mask row) and keeps the next row's chunks in flight while it
+// reduces the current one.  Per 16-byte chunk the mask is classified once per
+// batch entry: all 0 (add nothing), all -inf (the chunk is neither read nor
+// exponentiated; it is written as zeros) or mixed (added element by element).
+// Causal rows test keys against the query only in the chunk that holds the
+// diagonal; chunks wholly in the future are skipped like masked ones.
 // ----------------------------------------------------------------------------
-template <typename T, int TPR, int CPT>
-__global__ void __launch_bounds__(TPR <= 32 ? 256 : TPR)
+enum : uint32_t { kChunkPlain = 0u, kChunkSkip = 1u, kChunkMixed = 2u };
+
+// Mask class of a 16-byte chunk of T (2 bits).
+template <typename T>
+__device__ __forceinline__ uint32_t mask_chunk_class(const uint4 &m) {
+    using Tr = Traits<T>;
+    constexpr int V = Tr::kVec;
+    float mv[V];
+    Tr::unpack(m, mv);
+    bool all_zero = true, all_ninf = true;
+#pragma unroll
+    for (int e = 0; e < V; ++e) {
+        all_zero &= (mv[e] == 0.f);
+        all_ninf &= (mv[e] == -INFINITY);
+    }
+    return all_ninf ? kChunkSkip : (all_zero ? kChunkPlain : kChunkMixed);
+}
+
+// Position (batch entry, query) of consecutive rows, advanced without
+// division: rows of a row group are contiguous.
+struct RowPos {
+    int64_t b = 0, rem = 0, q = 0;
+    __device__ __forceinline__ void init(int64_t row, int64_t rows_per_batch, int64_t Tq) {
+        b = row / rows_per_batch;
+        rem = row - b * rows_per_batch;
+        q = row % Tq;
+    }
+    __device__ __forceinline__ void next(int64_t rows_per_batch, int64_t Tq) {
+        if (++rem == rows_per_batch) {
+            rem = 0;
+            ++b;
+        }
+        if (++q == Tq) q = 0;
+    }
+};
+
+// Shared memory of softmax_fw_vec: S stages of CPT 16-byte chunks per thread,
+// plus one word of chunk-class bits per thread and stage.
+template <int TPR, int CPT, int S>
+constexpr size_t softmax_fw_smem() {
+    return (size_t)S * (TPR <= 32 ? 256 : TPR) * (CPT * 16 + 4);
+}
+
+template <typename T, int TPR, int CPT, int S>
+__global__ void __launch_bounds__(TPR <= 32 ? 256 : TPR, (row_kernel_min_blocks<TPR, CPT>()))
 softmax_fw_vec(T *out, const T *inp, const T *mask, int64_t rows,
                int64_t rows_per_batch, int64_t Tq, int Tk, int causal) {
     using Tr = Traits<T>;
     constexpr int V = Tr::kVec;
+    constexpr int H2 = V / 2;
     constexpr int BLOCK = TPR <= 32 ? 256 : TPR;
-    constexpr int G = BLOCK / TPR;  // rows per block iteration
+    constexpr int G = BLOCK / TPR;  // row groups per block
+    static_assert(2 * CPT <= 32, "class bits");
+    extern __shared__ uint4 dsmem[];
+    uint4 *stage = dsmem;                                                  // [S][CPT][BLOCK]
+    uint32_t *clsb = reinterpret_cast<uint32_t *>(dsmem + S * CPT * BLOCK);  // [S][BLOCK]
     __shared__ float red[TPR > 32 ? 64 : 1];
 
-    const int lane = threadIdx.x % TPR;
-    const int grp = threadIdx.x / TPR;
+    const int tid = threadIdx.x;
+    const int lane = tid % TPR;
+    const int grp = tid / TPR;
     const int nchunk = Tk / V;
+    const int64_t ngroups = (int64_t)gridDim.x * G;
+    const int64_t per = (rows + ngroups - 1) / ngroups;  // rows per group (uniform)
+    const int64_t rbeg = ((int64_t)blockIdx.x * G + grp) * per;
+    const int64_t rend = rbeg + per < rows ? rbeg + per : rows;
+    const uint64_t pol = l2_evict_first_policy();
 
-    for (int64_t base = (int64_t)blockIdx.x * G; base < rows;
-         base += (int64_t)gridDim.x * G) {
-        const int64_t row = base + grp;
-        const bool valid = row < rows;
-        const int64_t qi = (valid && causal) ? row % Tq : (int64_t)Tk;
-        const T *xrow = inp + row * (int64_t)Tk;
-        const T *mrow = mask ? mask + (row / rows_per_batch) * (int64_t)Tk : nullptr;
-
-        float z[CPT][V];
-        float lmax = -INFINITY;
+    // mask classes of this thread's chunks for the cached batch entry
+    int64_t mb = -1;
+    uint32_t mcls = 0u;
+    auto chunk_classes = [&](int64_t b, int64_t q) -> uint32_t {
+        uint32_t cls = 0u;
+        if (mask) {
+            if (b != mb) {
+                mb = b;
+                mcls = 0u;
+                const T *mrow = mask + b * (int64_t)Tk;
 #pragma unroll
-        for (int k = 0; k < CPT; ++k) {
-            const int c = k * TPR + lane;
-            const int j0 = c * V;
-            bool live = valid && c < nchunk && (int64_t)j0 <= qi;
-            float mv[V];
-#pragma unroll
-            for (int e = 0; e < V; ++e) mv[e] = 0.f;
-            if (live && mrow) {
-                Tr::unpack(ld_cached16(mrow + j0), mv);
-                bool any = false;
-#pragma unroll
-                for (int e = 0; e < V; ++e) any |= (mv[e] != -INFINITY);
-                live = any;
-            }
-            if (live) {
-                float xv[V];
-                Tr::unpack(ld_stream16(xrow + j0), xv);
-#pragma unroll
-                for (int e = 0; e < V; ++e) {
-                    const bool future = (int64_t)(j0 + e) > qi;
-                    z[k][e] = future ? -INFINITY : (xv[e] + mv[e]) * kLog2e;
-                    lmax = fmaxf(lmax, z[k][e]);
+                for (int k = 0; k < CPT; ++k) {
+                    const int c = k * TPR + lane;
+                    if (c < nchunk)
+                        mcls |= mask_chunk_class<T>(ld_cached16(mrow + c * V)) << (2 * k);
                 }
-            } else {
+            }
+            cls = mcls;
+        }
+        if (causal) {  // future chunks skipped, the diagonal chunk mixed
+            const int qi = (int)q;
 #pragma unroll
-                for (int e = 0; e < V; ++e) z[k][e] = -INFINITY;
+            for (int k = 0; k < CPT; ++k) {
+                const int j0 = (k * TPR + lane) * V;
+                const uint32_t cur = (cls >> (2 * k)) & 3u;
+                uint32_t nc = cur;
+                if (j0 > qi) nc = kChunkSkip;
+                else if (j0 + V - 1 > qi && cur != kChunkSkip) nc = kChunkMixed;
+                cls = (cls & ~(3u << (2 * k))) | (nc << (2 * k));
             }
         }
-        float gmax = group_reduce<TPR, OpMax>(lmax, red);
-        if (gmax == -INFINITY) gmax = 0.f;  // fully masked row: every exp2 is 0
+        return cls;
+    };
 
-        float lsum = 0.f;
+    // Issue the copies of the next row into stage s (an empty group past the end).
+    RowPos ip;
+    if (rbeg < rend) ip.init(rbeg, rows_per_batch, Tq);
+    int64_t inext = rbeg;
+    auto issue = [&](int s) {
+        if (inext < rend) {
+            const uint32_t cls = chunk_classes(ip.b, ip.q);
+            clsb[s * BLOCK + tid] = cls;
+            const T *xrow = inp + inext * (int64_t)Tk;
 #pragma unroll
-        for (int k = 0; k < CPT; ++k) {
+            for (int k = 0; k < CPT; ++k) {
+                const int c = k * TPR + lane;
+                if (c < nchunk && ((cls >> (2 * k)) & 3u) != kChunkSkip)
+                    cp_async16(&stage[(s * CPT + k) * BLOCK + tid], xrow + c * V, pol);
+            }
+            ip.next(rows_per_batch, Tq);
+        }
+        ++inext;
+        cp_async_commit();
+    };
 #pragma unroll
-            for (int e = 0; e < V; ++e) {
-                z[k][e] = exp2f(z[k][e] - gmax);
-                lsum += z[k][e];
+    for (int s = 0; s < S - 1; ++s) issue(s);
+
+    RowPos cp;
+    if (rbeg < rend) cp.init(rbeg, rows_per_batch, Tq);
+    int s_cur = 0, s_iss = S - 1;
+    for (int64_t k = 0; k < per; ++k) {
+        issue(s_iss);
+        s_iss = s_iss + 1 == S ? 0 : s_iss + 1;
+        cp_async_wait<S - 1>();  // this thread's copies of row k have landed
+
+        const int64_t row = rbeg + k;
+        const bool valid = row < rend;
+        const uint32_t ccls = valid ? clsb[s_cur * BLOCK + tid] : 0u;
+        const int qi = (valid && causal) ? (int)cp.q : Tk;
+        const T *mrow = (valid && mask) ? mask + cp.b * (int64_t)Tk : nullptr;
+
+        float2 v[CPT][H2];
+        float m = -INFINITY;
+#pragma unroll
+        for (int kk = 0; kk < CPT; ++kk) {
+            const int c = kk * TPR + lane;
+            const uint32_t cls = (ccls >> (2 * kk)) & 3u;
+            if (valid && c < nchunk && cls != kChunkSkip) {
+                unpack2<T>(stage[(s_cur * CPT + kk) * BLOCK + tid], v[kk]);
+                if (cls == kChunkMixed) {
+                    float2 mv[H2];
+#pragma unroll
+                    for (int h = 0; h < H2; ++h) mv[h] = f2(0.f);
+                    if (mrow) unpack2<T>(ld_cached16(mrow + c * V), mv);
+#pragma unroll
+                    for (int h = 0; h < H2; ++h) {
+                        const int j = c * V + 2 * h;
+                        v[kk][h].x = j > qi ? -INFINITY : v[kk][h].x + mv[h].x;
+                        v[kk][h].y = j + 1 > qi ? -INFINITY : v[kk][h].y + mv[h].y;
+                    }
+                }
+#pragma unroll
+                for (int h = 0; h < H2; ++h) m = fmaxf(m, fmaxf(v[kk][h].x, v[kk][h].y));
             }
         }
-        const float gsum = group_reduce<TPR, OpSum>(lsum, red);
-        const float inv = gsum > 0.f ? 1.f / gsum : 0.f;
+        m = group_reduce<TPR, OpMax>(m, red);
+        // e = 2^(v*log2e - m*log2e); a row with no visible key sums to 0
+        const float mL = m == -INFINITY ? 0.f : m * kLog2e;
+        float2 sum2 = f2(0.f);
+#pragma unroll
+        for (int kk = 0; kk < CPT; ++kk) {
+            const int c = kk * TPR + lane;
+            const uint32_t cls = (ccls >> (2 * kk)) & 3u;
+            if (valid && c < nchunk && cls != kChunkSkip) {
+#pragma unroll
+                for (int h = 0; h < H2; ++h) {
+                    float2 t = __ffma2_rn(v[kk][h], f2(kLog2e), f2(-mL));
+                    t.x = fast_exp2(t.x);
+                    t.y = fast_exp2(t.y);
+                    v[kk][h] = t;
+                    sum2 = __fadd2_rn(sum2, t);
+                }
+            }
+        }
+        const float sum = group_reduce<TPR, OpSum>(sum2.x + sum2.y, red);
+        const float2 inv = f2(sum > 0.f ? 1.f / sum : 0.f);
 
         T *orow = out + row * (int64_t)Tk;
 #pragma unroll
-        for (int k = 0; k < CPT; ++k) {
-            const int c = k * TPR + lane;
+        for (int kk = 0; kk < CPT; ++kk) {
+            const int c = kk * TPR + lane;
+            const uint32_t cls = (ccls >> (2 * kk)) & 3u;
             if (valid && c < nchunk) {
-                float yv[V];
+                float2 yv[H2];
 #pragma unroll
-                for (int e = 0; e < V; ++e) yv[e] = z[k][e] * inv;
-                st_stream16(orow + c * V, Tr::pack(yv));
+                for (int h = 0; h < H2; ++h)
+                    yv[h] = cls == kChunkSkip ? f2(0.f) : __fmul2_rn(v[kk][h], inv);
+                st_stream16(orow + c * V, pack2<T>(yv));
             }
         }
+        if (valid) cp.next(rows_per_batch, Tq);
+        s_cur = s_cur + 1 == S ? 0 : s_cur + 1;
     }
 }
 

@@ -1,30 +1,39 @@
-"""Launch one kernel of the library a few times on one workload, for ncu.
+"""Launch (and optionally time) single kernels of the library on one workload.
 
     python -m transformer_reduce_gb300.profile_kernel KERNEL [--workload W] [--launches N]
+    python -m transformer_reduce_gb300.profile_kernel --sweep [--launches N]
 
 KERNEL is softmax_fw, softmax_bw, ln_fw, ln_dinp or ln_dgdb.  Only the
 buffers that kernel touches are allocated (for the encoder workload at most
-~0.8 GB), so a multi-pass ncu capture (which saves and restores device memory
-between passes) stays small, while the tensors still exceed L2 and the DRAM
-counters mean what they say.  This is a profiling driver, not a benchmark: it
-prints nothing but a line naming what it launched.
+~0.8 GB), so a multi-pass ncu capture, which saves and restores device memory
+between passes, stays small while the tensors still exceed L2.
+
+--sweep times every kernel on every workload of ``workloads`` (softmax: the
+tiny, GPT-2-small, length-sweep and encoder cases; LayerNorm: the tiny,
+GPT-2-small, width-sweep and encoder cases).  Each launch is timed alone with
+CUDA events on its stream, after an L2 flush (a write of 2x the L2 size); one
+JSON line per (kernel, workload) gives the median time and the algorithmic
+GB/s (``traffic``).  These are per-kernel context numbers; the benchmark
+proper is bench.py.
 """
 from __future__ import annotations
 
 import argparse
+import json
+import statistics
 
 import torch
 
-from . import _lib, build, workloads
+from . import _lib, build, traffic, workloads
 
 _DT = {"f32": _lib.LS_F32, "f16": _lib.LS_F16, "bf16": _lib.LS_BF16}
 
-WORKLOADS = {
-    "encoder_big": (workloads.ENCODER_BIG["softmax"], workloads.ENCODER_BIG["layernorm"][0]),
-    "gpt2_small": (workloads.GPT2_SMALL["softmax"], workloads.GPT2_SMALL["layernorm"]),
-    "softmax_T2048": (workloads.SOFTMAX_SWEEP[-1], None),
-    "layernorm_N8192": (None, workloads.LAYERNORM_SWEEP[-1]),
-}
+SOFTMAX_CASES = {c.name: c for c in
+                 [workloads.TINY["softmax"], workloads.GPT2_SMALL["softmax"],
+                  *workloads.SOFTMAX_SWEEP, workloads.ENCODER_BIG["softmax"]]}
+LN_CASES = {c.name: c for c in
+            [workloads.TINY["layernorm"], workloads.GPT2_SMALL["layernorm"],
+             *workloads.LAYERNORM_SWEEP, workloads.ENCODER_BIG["layernorm"][0]]}
 
 
 def _ok(s, where):
@@ -32,65 +41,123 @@ def _ok(s, where):
         raise _lib.LsError(s, where)
 
 
-def main(argv=None):
-    ap = argparse.ArgumentParser()
-    ap.add_argument("kernel", choices=["softmax_fw", "softmax_bw", "ln_fw", "ln_dinp", "ln_dgdb"])
-    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="encoder_big")
-    ap.add_argument("--launches", type=int, default=3)
-    a = ap.parse_args(argv)
-    build.build()
-    dev = torch.device("cuda", 0)
+def prepare(kernel: str, case, dev):
+    """(call, algorithmic bytes) for one kernel on one case; call() enqueues it."""
     st = torch.cuda.current_stream(dev).cuda_stream
-    sm_case, ln_case = WORKLOADS[a.workload]
-    calls = []
-    if a.kernel.startswith("softmax"):
-        s = sm_case
+    if kernel.startswith("softmax"):
+        s = case
         inp = workloads.softmax_inputs(s, device=dev)
         x, mask, dout = inp["scores"], inp["mask"], inp["dout"]
         m = 0 if mask is None else mask.data_ptr()
-        if a.kernel == "softmax_fw":
+        if kernel == "softmax_fw":
             y = torch.empty_like(x)
-            del dout
-            calls.append(lambda: _lib.ls_softmax_fw(y.data_ptr(), x.data_ptr(), m, s.B, s.H, s.T,
-                                                    s.T, s.causal, _DT[s.dtype], st))
-        else:
-            yf = workloads.softmax_probability_like(s, inp["lengths"], device=dev)
-            dx = torch.empty_like(x)
-            del x
-            calls.append(lambda: _lib.ls_softmax_bw(dx.data_ptr(), dout.data_ptr(), yf.data_ptr(),
-                                                    s.B, s.H, s.T, s.T, _DT[s.dtype], st))
+            nbytes = traffic.softmax_fw_bytes(s.B, s.H, s.T, inp["lengths"], s.causal, s.dtype,
+                                              mask is not None)
+            keep = (x, mask, y)
+            return (lambda: _lib.ls_softmax_fw(y.data_ptr(), x.data_ptr(), m, s.B, s.H, s.T, s.T,
+                                               s.causal, _DT[s.dtype], st)), nbytes, keep
+        yf = workloads.softmax_probability_like(s, inp["lengths"], device=dev)
+        dx = torch.empty_like(x)
+        keep = (dout, yf, dx)
+        return (lambda: _lib.ls_softmax_bw(dx.data_ptr(), dout.data_ptr(), yf.data_ptr(), s.B,
+                                           s.H, s.T, s.T, _DT[s.dtype], st)), \
+            traffic.softmax_bw_bytes(s.B, s.H, s.T, s.dtype), keep
+    c = case
+    li = workloads.layernorm_inputs(c, device=dev)
+    f32 = dict(device=dev, dtype=torch.float32)
+    mean = torch.full((c.rows,), c.x_mean, **f32)
+    rstd = torch.full((c.rows,), 1.0 / c.x_std, **f32)
+    if kernel == "ln_fw":
+        y = torch.empty_like(li["x"])
+        keep = (li, y, mean, rstd)
+        return (lambda: _lib.ls_layernorm_fw(
+            y.data_ptr(), mean.data_ptr(), rstd.data_ptr(), li["x"].data_ptr(),
+            li["gamma"].data_ptr(), li["beta"].data_ptr(), c.rows, c.hidden, c.eps,
+            _DT[c.dtype], st)), traffic.layernorm_fw_bytes(c.rows, c.hidden, c.dtype), keep
+    if kernel == "ln_dinp":
+        dx = torch.empty_like(li["x"])
+        keep = (li, dx, mean, rstd)
+        return (lambda: _lib.ls_layernorm_bw_dinp(
+            dx.data_ptr(), li["dy"].data_ptr(), li["x"].data_ptr(), li["gamma"].data_ptr(),
+            mean.data_ptr(), rstd.data_ptr(), c.rows, c.hidden, _DT[c.dtype], st)), \
+            traffic.layernorm_dinp_bytes(c.rows, c.hidden, c.dtype), keep
+    n = _lib.ls_layernorm_bw_dgamma_dbeta_workspace_size(c.rows, c.hidden)
+    ws = torch.empty(max(n, 16) // 4, **f32)
+    dg = torch.empty(c.hidden, **f32)
+    db = torch.empty(c.hidden, **f32)
+    keep = (li, ws, dg, db, mean, rstd)
+    return (lambda: _lib.ls_layernorm_bw_dgamma_dbeta(
+        dg.data_ptr(), db.data_ptr(), li["dy"].data_ptr(), li["x"].data_ptr(), mean.data_ptr(),
+        rstd.data_ptr(), c.rows, c.hidden, ws.data_ptr(), ws.numel() * 4, _DT[c.dtype], st)), \
+        traffic.layernorm_dgdb_bytes(c.rows, c.hidden, c.dtype), keep
+
+
+def time_kernel(call, launches: int, dev) -> list:
+    """Per-launch device times (ms), each launch after an L2 flush."""
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(2 * l2 // 4 + 1024, device=dev, dtype=torch.float32)
+    stream = torch.cuda.current_stream(dev)
+    out = []
+    for _ in range(launches + 2):
+        flush.fill_(1.0)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        _ok(call(), "kernel")
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        out.append(e0.elapsed_time(e1))
+    return out[2:]
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("kernel", nargs="?",
+                    choices=["softmax_fw", "softmax_bw", "ln_fw", "ln_dinp", "ln_dgdb"])
+    ap.add_argument("--workload", default="encoder_big",
+                    help="softmax or LayerNorm case name (encoder_big picks the encoder's case)")
+    ap.add_argument("--launches", type=int, default=3)
+    ap.add_argument("--sweep", action="store_true")
+    a = ap.parse_args(argv)
+    build.build()
+    dev = torch.device("cuda", 0)
+    if a.sweep:
+        peak = None
+        try:
+            import os
+            root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+            peak = json.load(open(os.path.join(root, "MEASURED_PEAKS.json")))["hbm_gbs"]
+        except Exception:
+            pass
+        jobs = [(k, c) for k in ("softmax_fw", "softmax_bw") for c in SOFTMAX_CASES.values()]
+        jobs += [(k, c) for k in ("ln_fw", "ln_dinp", "ln_dgdb") for c in LN_CASES.values()]
+        for kernel, case in jobs:
+            call, nbytes, keep = prepare(kernel, case, dev)
+            ms = time_kernel(call, max(a.launches, 5), dev)
+            med = statistics.median(ms)
+            gbs = nbytes / (med / 1e3) / 1e9
+            print(json.dumps({"kernel": kernel, "workload": case.name, "dtype": case.dtype,
+                              "median_us": round(med * 1e3, 2), "min_us": round(min(ms) * 1e3, 2),
+                              "bytes": nbytes, "gbs": round(gbs, 1),
+                              "frac_of_peak": round(gbs / peak, 4) if peak else None}),
+                  flush=True)
+            del keep, call
+            torch.cuda.empty_cache()
+        return
+    if a.kernel is None:
+        ap.error("KERNEL or --sweep is required")
+    if a.workload == "encoder_big":
+        case = workloads.ENCODER_BIG["softmax"] if a.kernel.startswith("softmax") \
+            else workloads.ENCODER_BIG["layernorm"][0]
     else:
-        c = ln_case
-        li = workloads.layernorm_inputs(c, device=dev)
-        f32 = dict(device=dev, dtype=torch.float32)
-        mean = torch.full((c.rows,), c.x_mean, **f32)
-        rstd = torch.full((c.rows,), 1.0 / c.x_std, **f32)
-        if a.kernel == "ln_fw":
-            y = torch.empty_like(li["x"])
-            calls.append(lambda: _lib.ls_layernorm_fw(
-                y.data_ptr(), mean.data_ptr(), rstd.data_ptr(), li["x"].data_ptr(),
-                li["gamma"].data_ptr(), li["beta"].data_ptr(), c.rows, c.hidden, c.eps,
-                _DT[c.dtype], st))
-        elif a.kernel == "ln_dinp":
-            dx = torch.empty_like(li["x"])
-            calls.append(lambda: _lib.ls_layernorm_bw_dinp(
-                dx.data_ptr(), li["dy"].data_ptr(), li["x"].data_ptr(), li["gamma"].data_ptr(),
-                mean.data_ptr(), rstd.data_ptr(), c.rows, c.hidden, _DT[c.dtype], st))
-        else:
-            n = _lib.ls_layernorm_bw_dgamma_dbeta_workspace_size(c.rows, c.hidden)
-            ws = torch.empty(max(n, 16) // 4, **f32)
-            dg = torch.empty(c.hidden, **f32)
-            db = torch.empty(c.hidden, **f32)
-            calls.append(lambda: _lib.ls_layernorm_bw_dgamma_dbeta(
-                dg.data_ptr(), db.data_ptr(), li["dy"].data_ptr(), li["x"].data_ptr(),
-                mean.data_ptr(), rstd.data_ptr(), c.rows, c.hidden, ws.data_ptr(),
-                ws.numel() * 4, _DT[c.dtype], st))
+        case = (SOFTMAX_CASES if a.kernel.startswith("softmax") else LN_CASES)[a.workload]
+    call, _, keep = prepare(a.kernel, case, dev)
     torch.cuda.synchronize(dev)
     for _ in range(a.launches):
-        for call in calls:
-            _ok(call(), a.kernel)
+        _ok(call(), a.kernel)
     torch.cuda.synchronize(dev)
-    print(f"profile_kernel: {a.kernel} x{a.launches} on {a.workload}")
+    del keep
+    print(f"profile_kernel: {a.kernel} x{a.launches} on {case.name}")
 
 
 if __name__ == "__main__":
