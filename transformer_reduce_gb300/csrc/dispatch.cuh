@@ -62,6 +62,41 @@ inline bool pick_bucket(int64_t nchunk, int maxcpt, int maxtpr, int *tpr, int *c
 
 constexpr int kMaxDevices = 64;
 
+// Bucket of the pipelined row kernels: as many chunks per thread as allowed
+// (maxcpt) and as few threads per row as that permits, so that per-row costs
+// (the shuffle reductions, the pipeline bookkeeping) are shared by as many
+// elements as possible and short rows pack several rows into one warp.
+inline bool pick_bucket_dense(int64_t nchunk, int maxcpt, int maxtpr, int *tpr, int *cpt) {
+    if (nchunk <= maxcpt) {
+        *tpr = 1;
+        *cpt = (int)(nchunk < 1 ? 1 : nchunk);
+        return true;
+    }
+    const int64_t t = next_pow2(ceil_div(nchunk, maxcpt));
+    if (t > maxtpr) return false;
+    *tpr = (int)t;
+    *cpt = (int)ceil_div(nchunk, t);
+    return true;
+}
+
+// Launch with programmatic stream serialisation (see pdl_begin): the kernel
+// may be scheduled while the previous kernel in the stream finishes.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*k)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                       Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, k, static_cast<KArgs>(args)...);
+}
+
 // Resident blocks per SM of one kernel instantiation with `smem` bytes of
 // dynamic shared memory (queried once; the opt-in above 48 KB is set once per
 // device before the first launch there).
@@ -91,8 +126,7 @@ cudaError_t launch_persistent(int block, size_t smem, int64_t work_blocks, cudaS
                               Args... args) {
     const int64_t cap = (int64_t)device_sm_count() * occupancy_per_sm<K>(block, smem);
     const int64_t grid = work_blocks < cap ? (work_blocks < 1 ? 1 : work_blocks) : cap;
-    K<<<(unsigned)grid, block, smem, st>>>(args...);
-    return cudaGetLastError();
+    return launch_pdl(K, dim3((unsigned)grid), dim3(block), smem, st, args...);
 }
 
 // Stages of the cp.async row pipelines (rows in flight per row group = S - 1).
@@ -103,15 +137,17 @@ constexpr int kLnDinpStages = 3;
 // ----------------------------------------------------------------------------
 // softmax
 // ----------------------------------------------------------------------------
-#define LSR_SOFTMAX_FW_BUCKETS(X)                                               \
-    X(1, 1) X(2, 1) X(4, 1) X(8, 1) X(16, 1) X(32, 1) X(32, 2) X(32, 3) X(32, 4) \
-    X(64, 4) X(128, 4) X(256, 4) X(512, 4)
+// (threads per row, chunks per thread) pairs pick_bucket_dense can return
+// with at most 4 chunks per thread.
+#define LSR_DENSE4_BUCKETS(X)                                                   \
+    X(1, 1) X(1, 2) X(1, 3) X(1, 4) X(2, 3) X(2, 4) X(4, 3) X(4, 4) X(8, 3)      \
+    X(8, 4) X(16, 3) X(16, 4) X(32, 3) X(32, 4) X(64, 3) X(64, 4) X(128, 3)      \
+    X(128, 4) X(256, 3) X(256, 4) X(512, 3) X(512, 4)
+#define LSR_SOFTMAX_FW_BUCKETS(X) LSR_DENSE4_BUCKETS(X)
 #define LSR_SOFTMAX_BW_BUCKETS(X)                                               \
     X(1, 1) X(2, 1) X(4, 1) X(8, 1) X(16, 1) X(32, 1) X(32, 2) X(32, 3) X(32, 4) \
     X(32, 5) X(32, 6) X(32, 7) X(32, 8) X(64, 8) X(128, 8) X(256, 8)
-#define LSR_LN_BUCKETS(X)                                                       \
-    X(1, 1) X(2, 1) X(4, 1) X(8, 1) X(16, 1) X(32, 1) X(32, 2) X(32, 3) X(32, 4) \
-    X(64, 4) X(128, 4) X(256, 4) X(512, 4)
+#define LSR_LN_BUCKETS(X) LSR_DENSE4_BUCKETS(X)
 
 template <typename T>
 cudaError_t launch_softmax_fw(T *out, const T *inp, const T *mask, int64_t rows,
@@ -119,7 +155,7 @@ cudaError_t launch_softmax_fw(T *out, const T *inp, const T *mask, int64_t rows,
                               int causal, bool vec, cudaStream_t st) {
     constexpr int V = Traits<T>::kVec;
     int tpr = 0, cpt = 0;
-    if (vec && pick_bucket(Tk / V, kSoftmaxFwMaxCpt, kSoftmaxFwMaxTpr, &tpr, &cpt)) {
+    if (vec && pick_bucket_dense(Tk / V, kSoftmaxFwMaxCpt, kSoftmaxFwMaxTpr, &tpr, &cpt)) {
 #define X(TPR_, CPT_)                                                                   \
     if (tpr == TPR_ && cpt == CPT_)                                                     \
         return launch_persistent<softmax_fw_vec<T, TPR_, CPT_, kSoftmaxFwStages>>(      \
@@ -166,7 +202,7 @@ cudaError_t launch_ln_fw(T *y, float *mean, float *rstd, const T *x, const T *ga
                          cudaStream_t st) {
     constexpr int V = Traits<T>::kVec;
     int tpr = 0, cpt = 0;
-    if (vec && pick_bucket(N / V, kLnMaxCpt, kLnMaxTpr, &tpr, &cpt)) {
+    if (vec && pick_bucket_dense(N / V, kLnMaxCpt, kLnMaxTpr, &tpr, &cpt)) {
 #define X(TPR_, CPT_)                                                                     \
     if (tpr == TPR_ && cpt == CPT_)                                                       \
         return launch_persistent<ln_fw_vec<T, TPR_, CPT_, kLnFwStages>>(                  \
@@ -189,7 +225,7 @@ cudaError_t launch_ln_dinp(T *dx, const T *dy, const T *x, const T *gamma,
                            int64_t N, bool vec, cudaStream_t st) {
     constexpr int V = Traits<T>::kVec;
     int tpr = 0, cpt = 0;
-    if (vec && pick_bucket(N / V, kLnMaxCpt, kLnMaxTpr, &tpr, &cpt)) {
+    if (vec && pick_bucket_dense(N / V, kLnMaxCpt, kLnMaxTpr, &tpr, &cpt)) {
 #define X(TPR_, CPT_)                                                                       \
     if (tpr == TPR_ && cpt == CPT_)                                                         \
         return launch_persistent<ln_dinp_vec<T, TPR_, CPT_, kLnDinpStages>>(                \
@@ -217,19 +253,19 @@ cudaError_t launch_ln_dgdb(float *dgamma, float *dbeta, const T *dy, const T *x,
         if (vec) {
             constexpr int V = Traits<T>::kVec;
             dim3 grid((unsigned)ceil_div(N, 32 * V), (unsigned)nchunks);
-            ln_dgdb_partial<T, V><<<grid, kDgdbWarps * 32, 0, st>>>(part, dy, x, mean, rstd,
-                                                                     rows, N, rpc);
+            cudaError_t e = launch_pdl(ln_dgdb_partial<T, V>, grid, dim3(kDgdbWarps * 32), 0, st,
+                                       part, dy, x, mean, rstd, rows, N, rpc);
+            if (e != cudaSuccess) return e;
         } else {
             dim3 grid((unsigned)ceil_div(N, 32), (unsigned)nchunks);
-            ln_dgdb_partial<T, 1><<<grid, kDgdbWarps * 32, 0, st>>>(part, dy, x, mean, rstd,
-                                                                     rows, N, rpc);
+            cudaError_t e = launch_pdl(ln_dgdb_partial<T, 1>, grid, dim3(kDgdbWarps * 32), 0, st,
+                                       part, dy, x, mean, rstd, rows, N, rpc);
+            if (e != cudaSuccess) return e;
         }
-        cudaError_t e = cudaGetLastError();
-        if (e != cudaSuccess) return e;
     }
-    ln_dgdb_final<<<(unsigned)ceil_div(N, kFinalCols), kFinalCols * kFinalLanes, 0, st>>>(
-        dgamma, dbeta, part, nchunks, N);
-    return cudaGetLastError();
+    return launch_pdl(ln_dgdb_final, dim3((unsigned)ceil_div(N, kFinalCols)),
+                      dim3(kFinalCols * kFinalLanes), 0, st, dgamma, dbeta,
+                      (const float *)part, nchunks, N);
 }
 
 #define LSR_INSTANTIATE(T)                                                                      \

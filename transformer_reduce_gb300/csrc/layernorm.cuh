@@ -61,6 +61,7 @@ template <typename T, int TPR, int CPT, int S>
 __global__ void __launch_bounds__(TPR <= 32 ? 256 : TPR, (row_kernel_min_blocks<TPR, CPT>()))
 ln_fw_vec(T *y, float *mean, float *rstd, const T *x, const T *gamma,
           const T *beta, int64_t rows, int N, float eps) {
+    pdl_begin();
     using Tr = Traits<T>;
     constexpr int V = Tr::kVec;
     constexpr int H2 = V / 2;
@@ -171,6 +172,7 @@ template <typename T, int TPR, int CPT, int S>
 __global__ void __launch_bounds__(TPR <= 32 ? 256 : TPR, (row_kernel_min_blocks<TPR, CPT>()))
 ln_dinp_vec(T *dx, const T *dy, const T *x, const T *gamma, const float *mean,
             const float *rstd, int64_t rows, int N) {
+    pdl_begin();
     using Tr = Traits<T>;
     constexpr int V = Tr::kVec;
     constexpr int H2 = V / 2;
@@ -276,6 +278,7 @@ template <typename T, int TPR>
 __global__ void __launch_bounds__(TPR <= 32 ? 256 : TPR)
 ln_fw_loop(T *y, float *mean, float *rstd, const T *x, const T *gamma,
            const T *beta, int64_t rows, int64_t N, float eps) {
+    pdl_begin();
     using Tr = Traits<T>;
     constexpr int BLOCK = TPR <= 32 ? 256 : TPR;
     constexpr int G = BLOCK / TPR;
@@ -320,6 +323,7 @@ template <typename T, int TPR>
 __global__ void __launch_bounds__(TPR <= 32 ? 256 : TPR)
 ln_dinp_loop(T *dx, const T *dy, const T *x, const T *gamma, const float *mean,
              const float *rstd, int64_t rows, int64_t N) {
+    pdl_begin();
     using Tr = Traits<T>;
     constexpr int BLOCK = TPR <= 32 ? 256 : TPR;
     constexpr int G = BLOCK / TPR;
@@ -370,6 +374,7 @@ template <typename T, int V>
 __global__ void __launch_bounds__(kDgdbWarps * 32, 4)
 ln_dgdb_partial(float *part, const T *dy, const T *x, const float *mean,
                 const float *rstd, int64_t rows, int64_t N, int64_t rows_per_chunk) {
+    pdl_begin();
     using Tr = Traits<T>;
     constexpr int CT = 32 * V;  // columns per tile
     __shared__ float sg[kDgdbWarps][CT];
@@ -477,6 +482,7 @@ constexpr int kFinalLanes = 8;
 
 static __global__ void __launch_bounds__(kFinalCols * kFinalLanes)
 ln_dgdb_final(float *dgamma, float *dbeta, const float *part, int64_t nchunks, int64_t N) {
+    pdl_begin();
     __shared__ float sg[kFinalLanes][kFinalCols];
     __shared__ float sb[kFinalLanes][kFinalCols];
     const int tx = threadIdx.x % kFinalCols;

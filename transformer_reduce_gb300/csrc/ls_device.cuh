@@ -149,6 +149,22 @@ __device__ __forceinline__ uint4 pack2<__nv_bfloat16>(const float2 (&f)[4]) {
 __device__ __forceinline__ float2 f2(float a) { return make_float2(a, a); }
 
 // ----------------------------------------------------------------------------
+// Programmatic dependent launch (sm_90+).  Every kernel of the library starts
+// by allowing the next kernel in the stream to be scheduled (its blocks can
+// then take over SM resources as this grid's blocks retire, instead of after
+// the whole grid has drained) and then waits, before its first global memory
+// access, until the previous grid has completed and its writes are visible.
+// Both are hardware operations that always complete (no spin loop); without
+// the launch attribute they are no-ops.  A dependent grid is only launched
+// once every block of this grid is resident or done, so waiting blocks can
+// never keep this grid's own blocks from running.
+// ----------------------------------------------------------------------------
+__device__ __forceinline__ void pdl_begin() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// ----------------------------------------------------------------------------
 // Asynchronous global -> shared copies (cp.async, sm_80+).  Each thread copies
 // its own 16-byte chunks into its own shared-memory slots and later reads only
 // those slots, so `cp.async.wait_group` (which waits for the calling thread's
@@ -201,6 +217,12 @@ __device__ __forceinline__ void st_stream16(void *p, const uint4 &v) {
 template <int TPR, int CPT>
 constexpr int row_kernel_min_blocks() {
     return TPR <= 32 ? (CPT <= 2 ? 4 : 2) : (512 / TPR > 0 ? 512 / TPR : 1);
+}
+// The softmax forward holds fewer values per chunk: 85 registers for 3-4
+// chunks (3 blocks of 256 threads).
+template <int TPR, int CPT>
+constexpr int softmax_fw_min_blocks() {
+    return TPR <= 32 ? (CPT <= 2 ? 4 : 3) : (512 / TPR > 0 ? 512 / TPR : 1);
 }
 
 // ----------------------------------------------------------------------------

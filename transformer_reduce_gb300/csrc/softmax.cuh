@@ -83,9 +83,10 @@ constexpr size_t softmax_fw_smem() {
 }
 
 template <typename T, int TPR, int CPT, int S>
-__global__ void __launch_bounds__(TPR <= 32 ? 256 : TPR, (row_kernel_min_blocks<TPR, CPT>()))
+__global__ void __launch_bounds__(TPR <= 32 ? 256 : TPR, (softmax_fw_min_blocks<TPR, CPT>()))
 softmax_fw_vec(T *out, const T *inp, const T *mask, int64_t rows,
                int64_t rows_per_batch, int64_t Tq, int Tk, int causal) {
+    pdl_begin();
     using Tr = Traits<T>;
     constexpr int V = Tr::kVec;
     constexpr int H2 = V / 2;
@@ -248,6 +249,7 @@ softmax_fw_vec(T *out, const T *inp, const T *mask, int64_t rows,
 template <typename T, int TPR, int CPT>
 __global__ void __launch_bounds__(TPR <= 32 ? 256 : TPR)
 softmax_bw_vec(T *dinp, const T *dout, const T *y, int64_t rows, int Tk) {
+    pdl_begin();
     using Tr = Traits<T>;
     constexpr int V = Tr::kVec;
     constexpr int BLOCK = TPR <= 32 ? 256 : TPR;
@@ -309,6 +311,7 @@ template <typename T, int TPR>
 __global__ void __launch_bounds__(TPR <= 32 ? 256 : TPR)
 softmax_fw_loop(T *out, const T *inp, const T *mask, int64_t rows,
                 int64_t rows_per_batch, int64_t Tq, int64_t Tk, int causal) {
+    pdl_begin();
     using Tr = Traits<T>;
     constexpr int BLOCK = TPR <= 32 ? 256 : TPR;
     constexpr int G = BLOCK / TPR;
@@ -359,6 +362,7 @@ softmax_fw_loop(T *out, const T *inp, const T *mask, int64_t rows,
 template <typename T, int TPR>
 __global__ void __launch_bounds__(TPR <= 32 ? 256 : TPR)
 softmax_bw_loop(T *dinp, const T *dout, const T *y, int64_t rows, int64_t Tk) {
+    pdl_begin();
     using Tr = Traits<T>;
     constexpr int BLOCK = TPR <= 32 ? 256 : TPR;
     constexpr int G = BLOCK / TPR;
