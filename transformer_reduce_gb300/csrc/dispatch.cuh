@@ -101,14 +101,19 @@ cudaError_t launch_pdl(void (*k)(KArgs...), dim3 grid, dim3 block, size_t smem, 
 // dynamic shared memory (queried once; the opt-in above 48 KB is set once per
 // device before the first launch there).
 template <auto K>
-int occupancy_per_sm(int block, size_t smem) {
+void ensure_dynamic_smem(size_t smem) {
     static std::atomic<int> configured[kMaxDevices];
     int dev = 0;
-    if (cudaGetDevice(&dev) == cudaSuccess && dev >= 0 && dev < kMaxDevices &&
-        smem > 48 * 1024 && !configured[dev].load(std::memory_order_acquire)) {
+    if (smem > 48 * 1024 && cudaGetDevice(&dev) == cudaSuccess && dev >= 0 &&
+        dev < kMaxDevices && !configured[dev].load(std::memory_order_acquire)) {
         cudaFuncSetAttribute(K, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         configured[dev].store(1, std::memory_order_release);
     }
+}
+
+template <auto K>
+int occupancy_per_sm(int block, size_t smem) {
+    ensure_dynamic_smem<K>(smem);
     static const int occ = [block, smem] {
         int n = 0;
         if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, K, block, smem) != cudaSuccess ||

@@ -474,27 +474,40 @@ ln_dgdb_partial(float *part, const T *dy, const T *x, const float *mean,
 
 // ----------------------------------------------------------------------------
 // gamma / beta gradient, stage 2: sum the chunk partials in a fixed order.
-// Block = 32 columns x 8 chunk lanes; chunk lane t sums chunks t, t+8, ...;
-// the 8 lane sums are then added in lane order.  nchunks == 0 writes zeros.
+// Block = 32 columns x 32 chunk lanes; chunk lane t sums chunks t, t+32, ...
+// in increasing order, loading a batch of 8 of them at once (the kernel is
+// latency-bound: few bytes, many dependent rounds otherwise); the 32 lane
+// sums are then added in lane order.  nchunks == 0 writes zeros.
 // ----------------------------------------------------------------------------
 constexpr int kFinalCols = 32;
-constexpr int kFinalLanes = 8;
+constexpr int kFinalLanes = 32;
+constexpr int kFinalBatch = 8;
 
 static __global__ void __launch_bounds__(kFinalCols * kFinalLanes)
 ln_dgdb_final(float *dgamma, float *dbeta, const float *part, int64_t nchunks, int64_t N) {
     pdl_begin();
-    __shared__ float sg[kFinalLanes][kFinalCols];
-    __shared__ float sb[kFinalLanes][kFinalCols];
+    __shared__ float sg[kFinalLanes][kFinalCols + 1];
+    __shared__ float sb[kFinalLanes][kFinalCols + 1];
     const int tx = threadIdx.x % kFinalCols;
     const int ty = threadIdx.x / kFinalCols;
     const int64_t col = (int64_t)blockIdx.x * kFinalCols + tx;
     float a = 0.f, b = 0.f;
-    if (col < N)
-#pragma unroll 8
-        for (int64_t c = ty; c < nchunks; c += kFinalLanes) {
-            a += __ldcs(part + (c * 2 + 0) * N + col);
-            b += __ldcs(part + (c * 2 + 1) * N + col);
+    if (col < N) {
+        for (int64_t base = ty; base < nchunks; base += (int64_t)kFinalLanes * kFinalBatch) {
+            float va[kFinalBatch], vb[kFinalBatch];
+#pragma unroll
+            for (int u = 0; u < kFinalBatch; ++u) {
+                const int64_t c = base + (int64_t)u * kFinalLanes;
+                va[u] = c < nchunks ? __ldcs(part + (c * 2 + 0) * N + col) : 0.f;
+                vb[u] = c < nchunks ? __ldcs(part + (c * 2 + 1) * N + col) : 0.f;
+            }
+#pragma unroll
+            for (int u = 0; u < kFinalBatch; ++u) {
+                a += va[u];
+                b += vb[u];
+            }
         }
+    }
     sg[ty][tx] = a;
     sb[ty][tx] = b;
     __syncthreads();
