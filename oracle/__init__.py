@@ -66,6 +66,10 @@ def _load():
         lib.ref_softmax_fw.restype = None
         lib.ref_softmax_bw.argtypes = [dp, dp, dp, i64, i64]
         lib.ref_softmax_bw.restype = None
+        lib.ref_softmax_fw_offset.argtypes = [dp, dp, dp, ip, ip, i64, i64, ctypes.c_int, i64]
+        lib.ref_softmax_fw_offset.restype = None
+        lib.ref_softmax_bw_masked.argtypes = [dp, dp, dp, dp, ip, ip, i64, i64, ctypes.c_int, i64]
+        lib.ref_softmax_bw_masked.restype = None
         lib.ref_layernorm_fw.argtypes = [dp, dp, dp, dp, dp, dp, i64, i64,
                                          ctypes.c_double]
         lib.ref_layernorm_fw.restype = None
@@ -145,6 +149,63 @@ def softmax_bw(dy, y):
     dx = np.empty_like(dy)
     _load().ref_softmax_bw(_ptr(dx), _ptr(dy), _ptr(y), nrows, tk)
     return dx
+
+
+def _rows_meta(nrows, mask, batch, query, causal):
+    if mask is not None:
+        batch = np.ascontiguousarray(np.asarray(batch, dtype=np.int64))
+        assert batch.shape == (nrows,)
+        assert batch.size == 0 or (batch.min() >= 0 and batch.max() < mask.shape[0])
+    if causal:
+        query = np.ascontiguousarray(np.asarray(query, dtype=np.int64))
+        assert query.shape == (nrows,)
+    return (_ptr(batch if mask is not None else None, ctypes.c_int64),
+            _ptr(query if causal else None, ctypes.c_int64), batch, query)
+
+
+def softmax_fw_offset(x, mask=None, batch=None, query=None, causal=False, offset=0):
+    """Softmax forward, causal keys visible up to query + offset (Tk - Tq)."""
+    x = _f64(x)
+    nrows, tk = x.shape
+    m = _f64(mask)
+    pb, pq, batch, query = _rows_meta(nrows, m, batch, query, causal)
+    y = np.empty_like(x)
+    _load().ref_softmax_fw_offset(_ptr(y), _ptr(x), _ptr(m), pb, pq, nrows, tk,
+                                  int(bool(causal)), int(offset))
+    return y
+
+
+def softmax_fw_tensor_offset(x4, mask=None, causal=False):
+    """Softmax forward of [B,H,Tq,Tk], Tq <= Tk, bottom-right causal alignment."""
+    x4 = _f64(x4)
+    B, H, Tq, Tk = x4.shape
+    rows = np.arange(B * H * Tq, dtype=np.int64)
+    y = softmax_fw_offset(x4.reshape(-1, Tk), mask, batch=rows // (H * Tq), query=rows % Tq,
+                          causal=causal, offset=Tk - Tq)
+    return y.reshape(B, H, Tq, Tk)
+
+
+def softmax_bw_masked(dy, y, mask=None, batch=None, query=None, causal=False, offset=0):
+    """Softmax backward over the visible keys only (0 on masked / future keys)."""
+    dy, y = _f64(dy), _f64(y)
+    assert dy.shape == y.shape
+    nrows, tk = dy.shape
+    m = _f64(mask)
+    pb, pq, batch, query = _rows_meta(nrows, m, batch, query, causal)
+    dx = np.empty_like(dy)
+    _load().ref_softmax_bw_masked(_ptr(dx), _ptr(dy), _ptr(y), _ptr(m), pb, pq, nrows, tk,
+                                  int(bool(causal)), int(offset))
+    return dx
+
+
+def softmax_bw_masked_tensor(dy4, y4, mask=None, causal=False):
+    """Masked softmax backward of [B,H,Tq,Tk] tensors (bottom-right causal)."""
+    dy4, y4 = _f64(dy4), _f64(y4)
+    B, H, Tq, Tk = dy4.shape
+    rows = np.arange(B * H * Tq, dtype=np.int64)
+    dx = softmax_bw_masked(dy4.reshape(-1, Tk), y4.reshape(-1, Tk), mask, batch=rows // (H * Tq),
+                           query=rows % Tq, causal=causal, offset=Tk - Tq)
+    return dx.reshape(B, H, Tq, Tk)
 
 
 def layernorm_fw(x, gamma, beta, eps):

@@ -120,6 +120,94 @@ void ref_softmax_bw(double *dx, const double *dy, const double *y,
 }
 
 /* ------------------------------------------------------------------------ */
+/* Attention softmax, causal with Tq <= Tk, and the masked backward           */
+/* ------------------------------------------------------------------------ */
+/*
+ * Visibility of key j to a row: not masked (mask != -inf) and, when causal,
+ * not in the future.  With Tq queries over Tk >= Tq keys the queries are the
+ * LAST Tq positions of the key sequence (bottom-right alignment): query i
+ * sits at key position i + (Tk - Tq) and sees keys j <= i + (Tk - Tq).  For
+ * Tq == Tk this is the j <= i rule of ref_softmax_fw.
+ */
+static int visible(const double *mr, int64_t j, int64_t q, int64_t offset, int causal)
+{
+    if (causal && j > q + offset)
+        return 0;
+    if (mr && mr[j] == -INFINITY)
+        return 0;
+    return 1;
+}
+
+/*
+ * Softmax forward with a causal offset: as ref_softmax_fw, with future keys
+ * j > query[r] + offset.  offset = Tk - Tq.
+ */
+void ref_softmax_fw_offset(double *y, const double *x, const double *mask,
+                           const int64_t *batch, const int64_t *query,
+                           int64_t nrows, int64_t Tk, int causal,
+                           int64_t offset)
+{
+    for (int64_t r = 0; r < nrows; ++r) {
+        const double *xr = x + r * Tk;
+        double *yr = y + r * Tk;
+        const double *mr = mask ? mask + batch[r] * Tk : 0;
+        const int64_t q = causal ? query[r] : 0;
+        double m = -INFINITY;
+        for (int64_t j = 0; j < Tk; ++j) {
+            double z;
+            if (causal && j > q + offset)
+                z = -INFINITY;
+            else
+                z = xr[j] + (mr ? mr[j] : 0.0);
+            yr[j] = z;
+            if (z > m)
+                m = z;
+        }
+        if (m == -INFINITY) {
+            for (int64_t j = 0; j < Tk; ++j)
+                yr[j] = 0.0;
+            continue;
+        }
+        double s = 0.0;
+        for (int64_t j = 0; j < Tk; ++j) {
+            double e = exp(yr[j] - m);
+            yr[j] = e;
+            s += e;
+        }
+        for (int64_t j = 0; j < Tk; ++j)
+            yr[j] = yr[j] / s;
+    }
+}
+
+/*
+ * Softmax backward restricted to the visible keys:
+ *   s    = sum over visible k of y_k dy_k
+ *   dx_j = y_j (dy_j - s)   for visible j,   0 otherwise.
+ * When y is the forward output (exactly 0 on invisible keys) this equals
+ * ref_softmax_bw; the masked form lets a kernel skip reading y and dy on keys
+ * it knows are invisible.
+ */
+void ref_softmax_bw_masked(double *dx, const double *dy, const double *y,
+                           const double *mask, const int64_t *batch,
+                           const int64_t *query, int64_t nrows, int64_t Tk,
+                           int causal, int64_t offset)
+{
+    for (int64_t r = 0; r < nrows; ++r) {
+        const double *yr = y + r * Tk;
+        const double *dyr = dy + r * Tk;
+        double *dxr = dx + r * Tk;
+        const double *mr = mask ? mask + batch[r] * Tk : 0;
+        const int64_t q = causal ? query[r] : 0;
+        double s = 0.0;
+        for (int64_t k = 0; k < Tk; ++k)
+            if (visible(mr, k, q, offset, causal))
+                s += yr[k] * dyr[k];
+        for (int64_t j = 0; j < Tk; ++j)
+            dxr[j] = visible(mr, j, q, offset, causal) ? yr[j] * (dyr[j] - s) : 0.0;
+    }
+}
+
+/* ------------------------------------------------------------------------ */
 /* LayerNorm forward                                                         */
 /* ------------------------------------------------------------------------ */
 /*

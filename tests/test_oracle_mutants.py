@@ -41,6 +41,14 @@ MUTANTS = [
     ("dgamma_transposed", "dg += dy[r * N + j] * xhat;", "dg += x[r * N + j] * xhat;", 0),
     ("dbeta_weighted", "db += dy[r * N + j];", "db += dy[r * N + j] * xhat;", 0),
     ("one_pass_no_square", "s2 += x[j] * x[j];", "s2 += x[j];", 0),
+    ("offset_sign", "if (causal && j > q + offset)", "if (causal && j > q - offset)", 0),
+    ("visible_offset_dropped", "if (causal && j > q + offset)\n        return 0;",
+     "if (causal && j > q)\n        return 0;", 0),
+    ("fw_offset_dropped", "if (causal && j > q + offset)", "if (causal && j > q)", 1),
+    ("masked_bw_sum_all_keys", "if (visible(mr, k, q, offset, causal))\n                s += yr[k] * dyr[k];",
+     "s += yr[k] * dyr[k];", 0),
+    ("masked_bw_no_zeroing", "dxr[j] = visible(mr, j, q, offset, causal) ? yr[j] * (dyr[j] - s) : 0.0;",
+     "dxr[j] = yr[j] * (dyr[j] - s);", 0),
 ]
 
 

@@ -328,3 +328,84 @@ def test_layernorm_empty_rows(ref):
     dg, db = ref.layernorm_bw_dgamma_dbeta(np.zeros((0, 4)), np.zeros((0, 4)),
                                            np.zeros(0), np.zeros(0))
     assert np.all(dg == 0.0) and np.all(db == 0.0)
+
+
+# ----------------------------------------------------------------------------
+# causal with Tq < Tk (bottom-right alignment) and the masked backward
+# ----------------------------------------------------------------------------
+
+def test_softmax_fw_offset_is_the_tail_of_the_square_causal_problem(ref):
+    # Tq queries over Tk keys, bottom-right aligned, are the last Tq rows of
+    # the square causal problem over Tk keys (pinned above).
+    rng = np.random.default_rng(51)
+    Tq, Tk = 3, 7
+    x = rng.normal(0, 2, size=(Tq, Tk))
+    sq = rng.normal(0, 2, size=(Tk, Tk))
+    sq[Tk - Tq:] = x
+    mask = _padding_mask([6], Tk)
+    want = ref.softmax_fw(sq, mask, batch=np.zeros(Tk, np.int64), query=np.arange(Tk),
+                          causal=True)[Tk - Tq:]
+    got = ref.softmax_fw_offset(x, mask, batch=np.zeros(Tq, np.int64), query=np.arange(Tq),
+                                causal=True, offset=Tk - Tq)
+    np.testing.assert_array_equal(got, want)
+    # offset 0 on a square problem is the plain causal forward
+    y0 = ref.softmax_fw_offset(sq, mask, batch=np.zeros(Tk, np.int64), query=np.arange(Tk),
+                               causal=True, offset=0)
+    np.testing.assert_array_equal(
+        y0, ref.softmax_fw(sq, mask, batch=np.zeros(Tk, np.int64), query=np.arange(Tk), causal=True))
+
+
+def test_softmax_bw_masked_central_differences(ref):
+    rng = np.random.default_rng(52)
+    B, H, Tq, Tk = 2, 1, 3, 5
+    x = rng.normal(0, 1, size=(B, H, Tq, Tk))
+    dy = rng.normal(0, 1, size=(B, H, Tq, Tk))
+    mask = _padding_mask([4, 5], Tk)
+
+    def loss(xx):
+        return float(np.sum(dy * ref.softmax_fw_tensor_offset(xx, mask, causal=True)))
+
+    y = ref.softmax_fw_tensor_offset(x, mask, causal=True)
+    dx = ref.softmax_bw_masked_tensor(dy, y, mask, causal=True)
+    h = 1e-6
+    fd = np.zeros_like(x)
+    for idx in np.ndindex(x.shape):
+        xp, xm = x.copy(), x.copy()
+        xp[idx] += h
+        xm[idx] -= h
+        fd[idx] = (loss(xp) - loss(xm)) / (2 * h)
+    assert np.max(np.abs(dx - fd)) <= 1e-6 * np.max(np.abs(fd))
+
+
+def test_softmax_bw_masked_matches_torch_autograd(ref):
+    rng = np.random.default_rng(53)
+    B, H, Tq, Tk = 2, 2, 4, 6
+    x = torch.tensor(rng.normal(0, 2, size=(B, H, Tq, Tk)), requires_grad=True)
+    dy = torch.tensor(rng.normal(0, 1, size=(B, H, Tq, Tk)))
+    mask = torch.tensor(_padding_mask([6, 4], Tk))
+    i = torch.arange(Tq).view(Tq, 1)
+    j = torch.arange(Tk).view(1, Tk)
+    future = torch.where(j > i + (Tk - Tq), -math.inf, 0.0).to(torch.float64)
+    y = torch.softmax(x + mask[:, None, None, :] + future, dim=-1)
+    y.backward(dy)
+    yo = ref.softmax_fw_tensor_offset(x.detach().numpy(), mask.numpy(), causal=True)
+    np.testing.assert_allclose(yo, y.detach().numpy(), rtol=1e-13, atol=1e-16)
+    dx = ref.softmax_bw_masked_tensor(dy.numpy(), yo, mask.numpy(), causal=True)
+    np.testing.assert_allclose(dx, x.grad.numpy(), rtol=1e-12, atol=1e-15)
+
+
+def test_softmax_bw_masked_ignores_invisible_inputs(ref):
+    # Garbage in y / dy at invisible keys changes nothing and gives exact zeros.
+    rng = np.random.default_rng(54)
+    B, H, Tq, Tk = 2, 2, 5, 5
+    mask = _padding_mask([3, 5], Tk)
+    y = ref.softmax_fw_tensor_offset(rng.normal(size=(B, H, Tq, Tk)), mask, causal=True)
+    dy = rng.normal(size=(B, H, Tq, Tk))
+    invisible = (y == 0.0)
+    y_dirty, dy_dirty = y.copy(), dy.copy()
+    y_dirty[invisible] = rng.uniform(1, 2, size=int(invisible.sum()))
+    dy_dirty[invisible] = 1e6
+    dx = ref.softmax_bw_masked_tensor(dy_dirty, y_dirty, mask, causal=True)
+    assert np.all(dx[invisible] == 0.0)
+    np.testing.assert_allclose(dx, ref.softmax_bw(dy.reshape(-1, Tk), y.reshape(-1, Tk)).reshape(y.shape),
+                               rtol=1e-13, atol=1e-16)
