@@ -67,7 +67,7 @@ typedef enum ls_status {
 /*
  * Attention softmax forward ("Problem 1.1" of the HW4 page; slides 23-26 of
  * the L10 page).  For every row (b, h, i) of the score tensor:
- *     z_j = -inf                       if causal and j > i  (future key)
+ *     z_j = -inf                       if causal and j > i + (Tk - Tq)  (future key)
  *     z_j = inp[b,h,i,j] + mask[b,j]   otherwise
  *     out[b,h,i,j] = exp(z_j - max_k z_k) / sum_k exp(z_k - max_k z_k)
  * A row whose every key is -inf is written as zeros.
@@ -77,9 +77,12 @@ typedef enum ls_status {
  *   mask  [B,Tk] dt additive mask (0 = keep, -inf = padded key), device,
  *         read; NULL means no mask.  Shared by all heads and queries of a
  *         batch entry.  Keys whose mask is -inf are not read from `inp`.
- *   causal  nonzero: mask future keys j > i; requires Tq == Tk.
+ *   causal  nonzero: mask future keys.  Requires Tq <= Tk; the Tq queries are
+ *           the last Tq positions of the key sequence (bottom-right
+ *           alignment), so query i sees keys j <= i + (Tk - Tq); with
+ *           Tq == Tk that is j <= i.
  * Errors: LS_ERR_INVALID_ARG for NULL out/inp with a non-empty problem,
- * negative sizes, or causal with Tq != Tk; LS_ERR_UNSUPPORTED for Tk beyond
+ * negative sizes, or causal with Tq > Tk; LS_ERR_UNSUPPORTED for Tk beyond
  * LS_MAX_ROW_LENGTH or an unknown dtype.
  */
 ls_status ls_softmax_fw(void *out, const void *inp, const void *mask,
@@ -100,6 +103,28 @@ ls_status ls_softmax_fw(void *out, const void *inp, const void *mask,
 ls_status ls_softmax_bw(void *dinp, const void *dout, const void *out_fw,
                         int64_t B, int64_t H, int64_t Tq, int64_t Tk,
                         ls_dtype dt, void *stream);
+
+/*
+ * Attention softmax backward that skips invisible keys: the same result as
+ * ls_softmax_bw when `out_fw` is the forward output (0 on masked and future
+ * keys), but keys that are masked (mask == -inf) or in the causal future are
+ * neither read from `dout` / `out_fw` nor summed; their gradient is written
+ * as 0.  Per row:
+ *     s      = sum over visible k of out_k * dout_k
+ *     dinp_j = out_j * (dout_j - s)   on visible keys, 0 elsewhere
+ * It is the backward counterpart of ls_softmax_fw's read skipping (the L10
+ * page's slide 30 names the score gradient as the O(T^2) tensor of the
+ * attention backward).
+ *
+ *   dinp    [B,H,Tq,Tk] dt, device, written.  May equal `dout`.
+ *   dout, out_fw  [B,H,Tq,Tk] dt, device, read on visible keys only.
+ *   mask    [B,Tk] dt additive mask or NULL, as for ls_softmax_fw.
+ *   causal  as for ls_softmax_fw (Tq <= Tk, bottom-right alignment).
+ * Errors as for ls_softmax_fw.
+ */
+ls_status ls_softmax_bw_masked(void *dinp, const void *dout, const void *out_fw,
+                               const void *mask, int64_t B, int64_t H, int64_t Tq,
+                               int64_t Tk, int causal, ls_dtype dt, void *stream);
 
 /*
  * LayerNorm forward ("Problem 2.1" of the HW4 page; slide 21 of the L10

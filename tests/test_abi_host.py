@@ -64,7 +64,11 @@ def test_rejections_before_launch(abi):
     # negative sizes, missing pointers, causal with Tq != Tk
     assert abi.ls_softmax_fw(fake, fake, None, -1, 1, 4, 4, 0, F32) == abi.LS_ERR_INVALID_ARG
     assert abi.ls_softmax_fw(None, fake, None, 1, 1, 4, 4, 0, F32) == abi.LS_ERR_INVALID_ARG
-    assert abi.ls_softmax_fw(fake, fake, None, 1, 1, 3, 4, 1, F32) == abi.LS_ERR_INVALID_ARG
+    assert abi.ls_softmax_fw(fake, fake, None, 1, 1, 5, 4, 1, F32) == abi.LS_ERR_INVALID_ARG  # causal, Tq > Tk
+    assert abi.ls_softmax_bw_masked(fake, fake, fake, None, 1, 1, 5, 4, 1, F32) == abi.LS_ERR_INVALID_ARG
+    assert abi.ls_softmax_bw_masked(fake, None, fake, None, 1, 1, 4, 4, 0, F32) == abi.LS_ERR_INVALID_ARG
+    assert abi.ls_softmax_bw_masked(fake, fake, fake, fake + 2, 1, 1, 4, 4, 0, F32) == abi.LS_ERR_MISALIGNED
+    assert abi.ls_softmax_bw_masked(None, None, None, None, 0, 1, 4, 4, 1, BF16) == abi.LS_OK
     assert abi.ls_softmax_bw(fake, None, fake, 1, 1, 4, 4, F32) == abi.LS_ERR_INVALID_ARG
     # misaligned element pointers
     assert abi.ls_softmax_fw(fake + 2, fake, None, 1, 1, 4, 4, 0, F32) == abi.LS_ERR_MISALIGNED

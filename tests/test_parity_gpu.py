@@ -418,3 +418,81 @@ def test_outputs_stay_inside_their_buffers():
         torch.cuda.synchronize()
         for buf in (ybuf, dbuf, lybuf, mbuf, rbuf, dxbuf, gbuf, bbuf):
             assert torch.all(buf[:G] == -12345.0) and torch.all(buf[-G:] == -12345.0)
+
+
+# ----------------------------------------------------------------------------
+# causal with Tq < Tk, and the masked backward
+# ----------------------------------------------------------------------------
+
+def _rand_problem(B, H, Tq, Tk, dtype, seed, lengths=None):
+    g = torch.Generator(device=DEV).manual_seed(seed)
+    dt = _dt(dtype)
+    x = torch.randn(B, H, Tq, Tk, generator=g, device=DEV).mul(3).to(dt)
+    dout = torch.randn(B, H, Tq, Tk, generator=g, device=DEV).to(dt)
+    mask = None
+    if lengths is not None:
+        m = torch.zeros(B, Tk, device=DEV)
+        for b, n in enumerate(lengths):
+            m[b, n:] = -math.inf
+        mask = m.to(dt)
+    return x, dout, mask
+
+
+@pytest.mark.parametrize("dtype,shape", [("f32", (2, 3, 5, 9)), ("bf16", (1, 2, 64, 256)),
+                                         ("f16", (2, 2, 7, 37)), ("bf16", (1, 1, 40, 4096))])
+def test_softmax_fw_causal_with_fewer_queries(dtype, shape):
+    L = _L()
+    B, H, Tq, Tk = shape
+    x, _, mask = _rand_problem(B, H, Tq, Tk, dtype, 61, lengths=[Tk - 1] * B)
+    y = L.softmax_fw(x, mask, causal=True)
+    torch.cuda.synchronize()
+    ref = oracle.softmax_fw_tensor_offset(x.cpu(), mask.cpu(), causal=True)
+    compare(y, ref, dtype, f"causal Tq<Tk fw {shape}")
+    assert np.all(y.cpu().float().numpy()[ref == 0.0] == 0.0)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "f16", "bf16"])
+@pytest.mark.parametrize("shape,lengths,causal", [
+    ((2, 3, 16, 16), [9, 16], True),
+    ((2, 3, 16, 256), [200, 77], False),
+    ((2, 2, 40, 64), [64, 33], True),
+    ((1, 2, 8, 100), [61], True),        # ragged: looped path
+    ((1, 2, 4, 2048), [1500], False),
+    ((1, 1, 3, 5000), [4000], True),     # beyond the register buckets
+])
+def test_softmax_bw_masked_ignores_invisible_keys(dtype, shape, lengths, causal):
+    """The masked backward equals the oracle's masked backward, is exactly 0 on
+    invisible keys, and is unaffected by garbage there in out_fw and dout."""
+    L = _L()
+    B, H, Tq, Tk = shape
+    x, dout, mask = _rand_problem(B, H, Tq, Tk, dtype, 62, lengths)
+    yref = oracle.softmax_fw_tensor_offset(x.cpu(), mask.cpu(), causal=causal)
+    invisible = torch.from_numpy(yref == 0.0).to(DEV)
+    y = torch.from_numpy(yref).to(_dt(dtype)).to(DEV)
+    y_dirty = torch.where(invisible, torch.full_like(y, 7.0), y)
+    d_dirty = torch.where(invisible, torch.full_like(dout, -3.0), dout)
+    dx = L.softmax_bw_masked(d_dirty, y_dirty, mask, causal=causal)
+    torch.cuda.synchronize()
+    want = oracle.softmax_bw_masked_tensor(d_dirty.cpu(), y_dirty.cpu(), mask.cpu(), causal=causal)
+    compare(dx, want, dtype, f"masked bw {shape} causal={causal}")
+    assert torch.all(dx[invisible] == 0)
+    # with the forward's own zeros it is the plain backward
+    dx_plain = L.softmax_bw(dout, y)
+    torch.cuda.synchronize()
+    compare(dx_plain, oracle.softmax_bw(dout.reshape(-1, Tk).cpu(), y.reshape(-1, Tk).cpu()),
+            dtype, "plain bw on the same forward")
+
+
+def test_softmax_bw_masked_encoder_big_sampled():
+    """The Transformer-big encoder shape (padding mask), sampled rows."""
+    L = _L()
+    from transformer_reduce_gb300 import workloads as W
+    s = W.ENCODER_BIG["softmax"]
+    inp = W.softmax_inputs(s, device=DEV)
+    y = W.softmax_probability_like(s, inp["lengths"], device=DEV)
+    dx = L.softmax_bw_masked(inp["dout"], y, inp["mask"], causal=False)
+    torch.cuda.synchronize()
+    rows = sample_rows(s.rows, boundaries=[b * s.H * s.T for b in range(1, s.B)], seed=8)
+    want = oracle.softmax_bw_masked(take_rows(inp["dout"], rows), take_rows(y, rows),
+                                    inp["mask"].cpu(), batch=rows // (s.H * s.T))
+    compare(take_rows(dx, rows), want, s.dtype, "encoder masked bw")

@@ -13,13 +13,13 @@ from __future__ import annotations
 from ._lib import (LS_BF16, LS_ERR_CUDA, LS_ERR_INVALID_ARG, LS_ERR_MISALIGNED,  # noqa: F401
                    LS_ERR_UNSUPPORTED, LS_ERR_WORKSPACE, LS_F16, LS_F32, LS_OK, LsError,
                    ls_layernorm_bw_dgamma_dbeta, ls_layernorm_bw_dgamma_dbeta_workspace_size,
-                   ls_layernorm_bw_dinp, ls_layernorm_fw, ls_softmax_bw, ls_softmax_fw, load,
-                   status_string)
+                   ls_layernorm_bw_dinp, ls_layernorm_fw, ls_softmax_bw, ls_softmax_bw_masked,
+                   ls_softmax_fw, load, status_string)
 
 __all__ = [
-    "softmax_fw", "softmax_bw", "layernorm_fw", "layernorm_bw_dinp",
+    "softmax_fw", "softmax_bw", "softmax_bw_masked", "layernorm_fw", "layernorm_bw_dinp",
     "layernorm_bw_dgamma_dbeta", "dgamma_dbeta_workspace", "LsError", "load",
-    "ls_softmax_fw", "ls_softmax_bw", "ls_layernorm_fw", "ls_layernorm_bw_dinp",
+    "ls_softmax_fw", "ls_softmax_bw", "ls_softmax_bw_masked", "ls_layernorm_fw", "ls_layernorm_bw_dinp",
     "ls_layernorm_bw_dgamma_dbeta", "ls_layernorm_bw_dgamma_dbeta_workspace_size",
 ]
 
@@ -63,8 +63,8 @@ def _ok(status: int, where: str):
 
 def softmax_fw(scores, mask=None, causal: bool = False, out=None):
     """Softmax over the last axis of scores [B,H,Tq,Tk] plus an additive mask
-    [B,Tk] (broadcast over heads and queries), future keys j > i masked when
-    ``causal``.  ``out`` may be ``scores`` itself (in place)."""
+    [B,Tk] (broadcast over heads and queries), future keys j > i + Tk - Tq
+    masked when ``causal`` (Tq <= Tk).  ``out`` may be ``scores`` (in place)."""
     torch = _torch()
     if scores.dim() != 4:
         raise ValueError("scores must be [B, H, Tq, Tk]")
@@ -89,6 +89,22 @@ def softmax_bw(dout, out_fw, dinp=None):
     _dev(dout, out_fw, dinp)
     _ok(ls_softmax_bw(_ptr(dinp), _ptr(dout), _ptr(out_fw), B, H, Tq, Tk, ls_dtype(dout),
                       _stream(dout)), "ls_softmax_bw")
+    return dinp
+
+
+def softmax_bw_masked(dout, out_fw, mask=None, causal: bool = False, dinp=None):
+    """Softmax backward that reads only visible keys (mask != -inf, not in the
+    causal future) and writes 0 on the others."""
+    torch = _torch()
+    if dout.dim() != 4 or dout.shape != out_fw.shape or dout.dtype != out_fw.dtype:
+        raise ValueError("dout and out_fw must be [B, H, Tq, Tk] of one dtype")
+    B, H, Tq, Tk = dout.shape
+    if mask is not None and (tuple(mask.shape) != (B, Tk) or mask.dtype != dout.dtype):
+        raise ValueError("mask must be [B, Tk] with the gradients' dtype")
+    dinp = torch.empty_like(dout) if dinp is None else dinp
+    _dev(dout, out_fw, mask, dinp)
+    _ok(ls_softmax_bw_masked(_ptr(dinp), _ptr(dout), _ptr(out_fw), _ptr(mask), B, H, Tq, Tk,
+                             causal, ls_dtype(dout), _stream(dout)), "ls_softmax_bw_masked")
     return dinp
 
 

@@ -26,6 +26,7 @@ _VP, _I64, _INT, _F32, _SZ = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctyp
 SIGNATURES = {
     "ls_softmax_fw": ([_VP, _VP, _VP, _I64, _I64, _I64, _I64, _INT, _INT, _VP], _INT),
     "ls_softmax_bw": ([_VP, _VP, _VP, _I64, _I64, _I64, _I64, _INT, _VP], _INT),
+    "ls_softmax_bw_masked": ([_VP, _VP, _VP, _VP, _I64, _I64, _I64, _I64, _INT, _INT, _VP], _INT),
     "ls_layernorm_fw": ([_VP, _VP, _VP, _VP, _VP, _VP, _I64, _I64, _F32, _INT, _VP], _INT),
     "ls_layernorm_bw_dinp": ([_VP, _VP, _VP, _VP, _VP, _VP, _I64, _I64, _INT, _VP], _INT),
     "ls_layernorm_bw_dgamma_dbeta_workspace_size": ([_I64, _I64], _SZ),
@@ -75,6 +76,11 @@ def ls_softmax_fw(out, inp, mask, B, H, Tq, Tk, causal, dt, stream=0) -> int:
 
 def ls_softmax_bw(dinp, dout, out_fw, B, H, Tq, Tk, dt, stream=0) -> int:
     return load().ls_softmax_bw(dinp, dout, out_fw, B, H, Tq, Tk, dt, stream)
+
+
+def ls_softmax_bw_masked(dinp, dout, out_fw, mask, B, H, Tq, Tk, causal, dt, stream=0) -> int:
+    return load().ls_softmax_bw_masked(dinp, dout, out_fw, mask, B, H, Tq, Tk, int(bool(causal)),
+                                       dt, stream)
 
 
 def ls_layernorm_fw(y, mean, rstd, x, gamma, beta, rows, hidden, eps, dt, stream=0) -> int:

@@ -94,7 +94,7 @@ ls_status ls_softmax_fw(void *out, const void *inp, const void *mask, int64_t B,
     const size_t es = elem_size(dt);
     if (es == 0) return LS_ERR_UNSUPPORTED;
     if (B < 0 || H < 0 || Tq < 0 || Tk < 0) return LS_ERR_INVALID_ARG;
-    if (causal && Tq != Tk) return LS_ERR_INVALID_ARG;
+    if (causal && Tq > Tk) return LS_ERR_INVALID_ARG;
     if (Tk > LS_MAX_ROW_LENGTH) return LS_ERR_UNSUPPORTED;
     if (B == 0 || H == 0 || Tq == 0 || Tk == 0) return LS_OK;
     if (!out || !inp) return LS_ERR_INVALID_ARG;
@@ -109,15 +109,15 @@ ls_status ls_softmax_fw(void *out, const void *inp, const void *mask, int64_t B,
         case LS_F32:
             return from_cuda(lsr::launch_softmax_fw<float>(
                 (float *)out, (const float *)inp, (const float *)mask, rows, H * Tq, Tq, Tk,
-                causal ? 1 : 0, vec, st));
+                causal ? 1 : 0, Tk - Tq, vec, st));
         case LS_F16:
             return from_cuda(lsr::launch_softmax_fw<__half>(
                 (__half *)out, (const __half *)inp, (const __half *)mask, rows, H * Tq, Tq, Tk,
-                causal ? 1 : 0, vec, st));
+                causal ? 1 : 0, Tk - Tq, vec, st));
         case LS_BF16:
             return from_cuda(lsr::launch_softmax_fw<__nv_bfloat16>(
                 (__nv_bfloat16 *)out, (const __nv_bfloat16 *)inp, (const __nv_bfloat16 *)mask,
-                rows, H * Tq, Tq, Tk, causal ? 1 : 0, vec, st));
+                rows, H * Tq, Tq, Tk, causal ? 1 : 0, Tk - Tq, vec, st));
     }
     return LS_ERR_UNSUPPORTED;
 }
@@ -148,6 +148,43 @@ ls_status ls_softmax_bw(void *dinp, const void *dout, const void *out_fw, int64_
             return from_cuda(lsr::launch_softmax_bw<__nv_bfloat16>(
                 (__nv_bfloat16 *)dinp, (const __nv_bfloat16 *)dout,
                 (const __nv_bfloat16 *)out_fw, rows, Tk, vec, st));
+    }
+    return LS_ERR_UNSUPPORTED;
+}
+
+ls_status ls_softmax_bw_masked(void *dinp, const void *dout, const void *out_fw,
+                               const void *mask, int64_t B, int64_t H, int64_t Tq, int64_t Tk,
+                               int causal, ls_dtype dt, void *stream) {
+    const size_t es = elem_size(dt);
+    if (es == 0) return LS_ERR_UNSUPPORTED;
+    if (B < 0 || H < 0 || Tq < 0 || Tk < 0) return LS_ERR_INVALID_ARG;
+    if (causal && Tq > Tk) return LS_ERR_INVALID_ARG;
+    if (Tk > LS_MAX_ROW_LENGTH) return LS_ERR_UNSUPPORTED;
+    if (B == 0 || H == 0 || Tq == 0 || Tk == 0) return LS_OK;
+    if (!dinp || !dout || !out_fw) return LS_ERR_INVALID_ARG;
+    if (H > INT64_MAX / B || Tq > INT64_MAX / (B * H) || Tk > INT64_MAX / (B * H * Tq))
+        return LS_ERR_UNSUPPORTED;
+    if (!aligned(dinp, es) || !aligned(dout, es) || !aligned(out_fw, es) ||
+        (mask && !aligned(mask, es)))
+        return LS_ERR_MISALIGNED;
+    const int64_t rows = B * H * Tq;
+    const bool vec = vec_ok(Tk, es, {dinp, dout, out_fw, mask});
+    const int c = causal ? 1 : 0;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    switch (dt) {
+        case LS_F32:
+            return from_cuda(lsr::launch_softmax_bw_masked<float>(
+                (float *)dinp, (const float *)dout, (const float *)out_fw, (const float *)mask,
+                rows, H * Tq, Tq, Tk, c, Tk - Tq, vec, st));
+        case LS_F16:
+            return from_cuda(lsr::launch_softmax_bw_masked<__half>(
+                (__half *)dinp, (const __half *)dout, (const __half *)out_fw,
+                (const __half *)mask, rows, H * Tq, Tq, Tk, c, Tk - Tq, vec, st));
+        case LS_BF16:
+            return from_cuda(lsr::launch_softmax_bw_masked<__nv_bfloat16>(
+                (__nv_bfloat16 *)dinp, (const __nv_bfloat16 *)dout,
+                (const __nv_bfloat16 *)out_fw, (const __nv_bfloat16 *)mask, rows, H * Tq, Tq,
+                Tk, c, Tk - Tq, vec, st));
     }
     return LS_ERR_UNSUPPORTED;
 }

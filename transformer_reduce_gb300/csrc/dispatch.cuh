@@ -157,7 +157,7 @@ constexpr int kLnDinpStages = 3;
 template <typename T>
 cudaError_t launch_softmax_fw(T *out, const T *inp, const T *mask, int64_t rows,
                               int64_t rows_per_batch, int64_t Tq, int64_t Tk,
-                              int causal, bool vec, cudaStream_t st) {
+                              int causal, int64_t qoff, bool vec, cudaStream_t st) {
     constexpr int V = Traits<T>::kVec;
     int tpr = 0, cpt = 0;
     if (vec && pick_bucket_dense(Tk / V, kSoftmaxFwMaxCpt, kSoftmaxFwMaxTpr, &tpr, &cpt)) {
@@ -166,16 +166,16 @@ cudaError_t launch_softmax_fw(T *out, const T *inp, const T *mask, int64_t rows,
         return launch_persistent<softmax_fw_vec<T, TPR_, CPT_, kSoftmaxFwStages>>(      \
             block_threads<TPR_>(), softmax_fw_smem<TPR_, CPT_, kSoftmaxFwStages>(),        \
             ceil_div(rows, rows_per_block<TPR_>()), st, out, inp, mask, rows,               \
-            rows_per_batch, Tq, (int)Tk, causal);
+            rows_per_batch, Tq, (int)Tk, causal, qoff);
         LSR_SOFTMAX_FW_BUCKETS(X)
 #undef X
     }
     if (Tk <= kLoopWarpRowMax)
         return launch_persistent<softmax_fw_loop<T, 32>>(256, 0, ceil_div(rows, 8), st, out, inp,
                                                          mask, rows, rows_per_batch, Tq, Tk,
-                                                         causal);
+                                                         causal, qoff);
     return launch_persistent<softmax_fw_loop<T, 256>>(256, 0, rows, st, out, inp, mask, rows,
-                                                      rows_per_batch, Tq, Tk, causal);
+                                                      rows_per_batch, Tq, Tk, causal, qoff);
 }
 
 template <typename T>
@@ -196,6 +196,30 @@ cudaError_t launch_softmax_bw(T *dinp, const T *dout, const T *y, int64_t rows,
         return launch_persistent<softmax_bw_loop<T, 32>>(256, 0, ceil_div(rows, 8), st, dinp, dout,
                                                          y, rows, Tk);
     return launch_persistent<softmax_bw_loop<T, 256>>(256, 0, rows, st, dinp, dout, y, rows, Tk);
+}
+
+template <typename T>
+cudaError_t launch_softmax_bw_masked(T *dinp, const T *dout, const T *y, const T *mask,
+                                     int64_t rows, int64_t rows_per_batch, int64_t Tq,
+                                     int64_t Tk, int causal, int64_t qoff, bool vec,
+                                     cudaStream_t st) {
+    constexpr int V = Traits<T>::kVec;
+    int tpr = 0, cpt = 0;
+    if (vec && pick_bucket(Tk / V, kSoftmaxBwMaxCpt, kSoftmaxBwMaxTpr, &tpr, &cpt)) {
+#define X(TPR_, CPT_)                                                                   \
+    if (tpr == TPR_ && cpt == CPT_)                                                     \
+        return launch_persistent<softmax_bw_masked_vec<T, TPR_, CPT_>>(                 \
+            block_threads<TPR_>(), 0, ceil_div(rows, rows_per_block<TPR_>()), st, dinp,     \
+            dout, y, mask, rows, rows_per_batch, Tq, (int)Tk, causal, qoff);
+        LSR_SOFTMAX_BW_BUCKETS(X)
+#undef X
+    }
+    if (Tk <= kLoopWarpRowMax)
+        return launch_persistent<softmax_bw_masked_loop<T, 32>>(
+            256, 0, ceil_div(rows, 8), st, dinp, dout, y, mask, rows, rows_per_batch, Tq, Tk,
+            causal, qoff);
+    return launch_persistent<softmax_bw_masked_loop<T, 256>>(
+        256, 0, rows, st, dinp, dout, y, mask, rows, rows_per_batch, Tq, Tk, causal, qoff);
 }
 
 // ----------------------------------------------------------------------------
@@ -275,7 +299,11 @@ cudaError_t launch_ln_dgdb(float *dgamma, float *dbeta, const T *dy, const T *x,
 
 #define LSR_INSTANTIATE(T)                                                                      \
     template cudaError_t launch_softmax_fw<T>(T *, const T *, const T *, int64_t, int64_t,     \
-                                              int64_t, int64_t, int, bool, cudaStream_t);      \
+                                              int64_t, int64_t, int, int64_t, bool,            \
+                                              cudaStream_t);                                   \
+    template cudaError_t launch_softmax_bw_masked<T>(T *, const T *, const T *, const T *,     \
+                                                     int64_t, int64_t, int64_t, int64_t, int,  \
+                                                     int64_t, bool, cudaStream_t);             \
     template cudaError_t launch_softmax_bw<T>(T *, const T *, const T *, int64_t, int64_t,     \
                                               bool, cudaStream_t);                             \
     template cudaError_t launch_ln_fw<T>(T *, float *, float *, const T *, const T *,          \

@@ -57,6 +57,50 @@ __device__ __forceinline__ uint32_t mask_chunk_class(const uint4 &m) {
     return all_ninf ? kChunkSkip : (all_zero ? kChunkPlain : kChunkMixed);
 }
 
+// Chunk classes (2 bits per chunk) of one thread's chunks for a row: the mask
+// classes of the row's batch entry (cached: consecutive rows usually share
+// it), then, when causal, chunks wholly after the last visible key `qlim` are
+// skipped and the chunk holding it is mixed.
+template <typename T, int TPR, int CPT>
+struct RowClasses {
+    const T *mask;
+    int Tk, nchunk, lane;
+    int64_t mb = -1;
+    uint32_t mcls = 0u;
+    __device__ __forceinline__ RowClasses(const T *m, int tk, int lane_)
+        : mask(m), Tk(tk), nchunk(tk / Traits<T>::kVec), lane(lane_) {}
+    __device__ __forceinline__ uint32_t get(int64_t b, int64_t qlim, int causal) {
+        constexpr int V = Traits<T>::kVec;
+        uint32_t cls = 0u;
+        if (mask) {
+            if (b != mb) {
+                mb = b;
+                mcls = 0u;
+                const T *mrow = mask + b * (int64_t)Tk;
+#pragma unroll
+                for (int k = 0; k < CPT; ++k) {
+                    const int c = k * TPR + lane;
+                    if (c < nchunk)
+                        mcls |= mask_chunk_class<T>(ld_cached16(mrow + c * V)) << (2 * k);
+                }
+            }
+            cls = mcls;
+        }
+        if (causal) {
+#pragma unroll
+            for (int k = 0; k < CPT; ++k) {
+                const int64_t j0 = (int64_t)(k * TPR + lane) * V;
+                const uint32_t cur = (cls >> (2 * k)) & 3u;
+                uint32_t nc = cur;
+                if (j0 > qlim) nc = kChunkSkip;
+                else if (j0 + V - 1 > qlim && cur != kChunkSkip) nc = kChunkMixed;
+                cls = (cls & ~(3u << (2 * k))) | (nc << (2 * k));
+            }
+        }
+        return cls;
+    }
+};
+
 // Position (batch entry, query) of consecutive rows, advanced without
 // division: rows of a row group are contiguous.
 struct RowPos {
@@ -85,7 +129,7 @@ constexpr size_t softmax_fw_smem() {
 template <typename T, int TPR, int CPT, int S>
 __global__ void __launch_bounds__(TPR <= 32 ? 256 : TPR, (softmax_fw_min_blocks<TPR, CPT>()))
 softmax_fw_vec(T *out, const T *inp, const T *mask, int64_t rows,
-               int64_t rows_per_batch, int64_t Tq, int Tk, int causal) {
+               int64_t rows_per_batch, int64_t Tq, int Tk, int causal, int64_t qoff) {
     pdl_begin();
     using Tr = Traits<T>;
     constexpr int V = Tr::kVec;
@@ -108,39 +152,7 @@ softmax_fw_vec(T *out, const T *inp, const T *mask, int64_t rows,
     const int64_t rend = rbeg + per < rows ? rbeg + per : rows;
     const uint64_t pol = l2_evict_first_policy();
 
-    // mask classes of this thread's chunks for the cached batch entry
-    int64_t mb = -1;
-    uint32_t mcls = 0u;
-    auto chunk_classes = [&](int64_t b, int64_t q) -> uint32_t {
-        uint32_t cls = 0u;
-        if (mask) {
-            if (b != mb) {
-                mb = b;
-                mcls = 0u;
-                const T *mrow = mask + b * (int64_t)Tk;
-#pragma unroll
-                for (int k = 0; k < CPT; ++k) {
-                    const int c = k * TPR + lane;
-                    if (c < nchunk)
-                        mcls |= mask_chunk_class<T>(ld_cached16(mrow + c * V)) << (2 * k);
-                }
-            }
-            cls = mcls;
-        }
-        if (causal) {  // future chunks skipped, the diagonal chunk mixed
-            const int qi = (int)q;
-#pragma unroll
-            for (int k = 0; k < CPT; ++k) {
-                const int j0 = (k * TPR + lane) * V;
-                const uint32_t cur = (cls >> (2 * k)) & 3u;
-                uint32_t nc = cur;
-                if (j0 > qi) nc = kChunkSkip;
-                else if (j0 + V - 1 > qi && cur != kChunkSkip) nc = kChunkMixed;
-                cls = (cls & ~(3u << (2 * k))) | (nc << (2 * k));
-            }
-        }
-        return cls;
-    };
+    RowClasses<T, TPR, CPT> classes(mask, Tk, lane);
 
     // Issue the copies of the next row into stage s (an empty group past the end).
     RowPos ip;
@@ -148,7 +160,7 @@ softmax_fw_vec(T *out, const T *inp, const T *mask, int64_t rows,
     int64_t inext = rbeg;
     auto issue = [&](int s) {
         if (inext < rend) {
-            const uint32_t cls = chunk_classes(ip.b, ip.q);
+            const uint32_t cls = classes.get(ip.b, ip.q + qoff, causal);
             clsb[s * BLOCK + tid] = cls;
             const T *xrow = inp + inext * (int64_t)Tk;
 #pragma unroll
@@ -176,7 +188,7 @@ softmax_fw_vec(T *out, const T *inp, const T *mask, int64_t rows,
         const int64_t row = rbeg + k;
         const bool valid = row < rend;
         const uint32_t ccls = valid ? clsb[s_cur * BLOCK + tid] : 0u;
-        const int qi = (valid && causal) ? (int)cp.q : Tk;
+        const int qi = (valid && causal) ? (int)(cp.q + qoff) : Tk;  // last visible key
         const T *mrow = (valid && mask) ? mask + cp.b * (int64_t)Tk : nullptr;
 
         float2 v[CPT][H2];
@@ -310,7 +322,7 @@ softmax_bw_vec(T *dinp, const T *dout, const T *y, int64_t rows, int Tk) {
 template <typename T, int TPR>
 __global__ void __launch_bounds__(TPR <= 32 ? 256 : TPR)
 softmax_fw_loop(T *out, const T *inp, const T *mask, int64_t rows,
-                int64_t rows_per_batch, int64_t Tq, int64_t Tk, int causal) {
+                int64_t rows_per_batch, int64_t Tq, int64_t Tk, int causal, int64_t qoff) {
     pdl_begin();
     using Tr = Traits<T>;
     constexpr int BLOCK = TPR <= 32 ? 256 : TPR;
@@ -323,7 +335,7 @@ softmax_fw_loop(T *out, const T *inp, const T *mask, int64_t rows,
          base += (int64_t)gridDim.x * G) {
         const int64_t row = base + grp;
         const bool valid = row < rows;
-        const int64_t qi = causal ? (valid ? row % Tq : 0) : Tk;
+        const int64_t qi = causal ? (valid ? row % Tq + qoff : 0) : Tk;  // last visible key
         const int64_t jend = valid ? (qi < Tk ? qi + 1 : Tk) : 0;  // keys past qi are future
         const T *xrow = inp + row * Tk;
         const T *mrow = mask ? mask + (row / rows_per_batch) * Tk : nullptr;
@@ -385,6 +397,147 @@ softmax_bw_loop(T *dinp, const T *dout, const T *y, int64_t rows, int64_t Tk) {
                 const float yv = Tr::load1(y + off + j);
                 const float gv = Tr::load1(dout + off + j);
                 Tr::store1(dinp + off + j, yv * (gv - s));
+            }
+    }
+}
+
+// ----------------------------------------------------------------------------
+// Masked backward: dinp_j = y_j (dout_j - sum over visible k of y_k dout_k)
+// on visible keys, 0 elsewhere.  Chunks whose keys are all invisible (mask
+// -inf, or causal future) are neither read nor summed; they are written as
+// zeros.  Same row mapping as softmax_bw_vec, rows of a group contiguous.
+// ----------------------------------------------------------------------------
+template <typename T, int TPR, int CPT>
+__global__ void __launch_bounds__(TPR <= 32 ? 256 : TPR)
+softmax_bw_masked_vec(T *dinp, const T *dout, const T *y, const T *mask, int64_t rows,
+                      int64_t rows_per_batch, int64_t Tq, int Tk, int causal, int64_t qoff) {
+    pdl_begin();
+    using Tr = Traits<T>;
+    constexpr int V = Tr::kVec;
+    constexpr int H2 = V / 2;
+    constexpr int BLOCK = TPR <= 32 ? 256 : TPR;
+    constexpr int G = BLOCK / TPR;
+    __shared__ float red[TPR > 32 ? 64 : 1];
+
+    const int lane = threadIdx.x % TPR;
+    const int grp = threadIdx.x / TPR;
+    const int nchunk = Tk / V;
+    const int64_t ngroups = (int64_t)gridDim.x * G;
+    const int64_t per = (rows + ngroups - 1) / ngroups;
+    const int64_t rbeg = ((int64_t)blockIdx.x * G + grp) * per;
+    const int64_t rend = rbeg + per < rows ? rbeg + per : rows;
+    RowClasses<T, TPR, CPT> classes(mask, Tk, lane);
+    RowPos pos;
+    if (rbeg < rend) pos.init(rbeg, rows_per_batch, Tq);
+
+    for (int64_t k = 0; k < per; ++k) {
+        const int64_t row = rbeg + k;
+        const bool valid = row < rend;
+        const int64_t off = row * (int64_t)Tk;
+        const uint32_t ccls = valid ? classes.get(pos.b, pos.q + qoff, causal) : 0u;
+        const int qi = (valid && causal) ? (int)(pos.q + qoff) : Tk;
+        const T *mrow = (valid && mask) ? mask + pos.b * (int64_t)Tk : nullptr;
+
+        uint4 yr[CPT], gr[CPT];
+#pragma unroll
+        for (int kk = 0; kk < CPT; ++kk) {
+            const int c = kk * TPR + lane;
+            const uint32_t cls = (ccls >> (2 * kk)) & 3u;
+            if (valid && c < nchunk && cls != kChunkSkip) {
+                yr[kk] = ld_stream16(y + off + c * V);
+                gr[kk] = ld_stream16(dout + off + c * V);
+            } else {
+                yr[kk] = make_uint4(0u, 0u, 0u, 0u);
+                gr[kk] = make_uint4(0u, 0u, 0u, 0u);
+            }
+        }
+        // visibility of the elements of mixed chunks (mask -inf or future)
+        uint32_t vis[CPT];
+#pragma unroll
+        for (int kk = 0; kk < CPT; ++kk) {
+            const int c = kk * TPR + lane;
+            const uint32_t cls = (ccls >> (2 * kk)) & 3u;
+            vis[kk] = cls == kChunkSkip ? 0u : (1u << V) - 1u;
+            if (valid && c < nchunk && cls == kChunkMixed) {
+                float mv[V];
+#pragma unroll
+                for (int e = 0; e < V; ++e) mv[e] = 0.f;
+                if (mrow) Tr::unpack(ld_cached16(mrow + c * V), mv);
+                uint32_t bits = 0u;
+#pragma unroll
+                for (int e = 0; e < V; ++e)
+                    if (mv[e] != -INFINITY && c * V + e <= qi) bits |= 1u << e;
+                vis[kk] = bits;
+            }
+        }
+        float2 s2 = f2(0.f);
+#pragma unroll
+        for (int kk = 0; kk < CPT; ++kk) {
+            float2 yv[H2], gv[H2];
+            unpack2<T>(yr[kk], yv);
+            unpack2<T>(gr[kk], gv);
+#pragma unroll
+            for (int h = 0; h < H2; ++h) {
+                const float2 p = __fmul2_rn(yv[h], gv[h]);
+                s2.x += (vis[kk] >> (2 * h)) & 1u ? p.x : 0.f;
+                s2.y += (vis[kk] >> (2 * h + 1)) & 1u ? p.y : 0.f;
+            }
+        }
+        const float s = group_reduce<TPR, OpSum>(s2.x + s2.y, red);
+#pragma unroll
+        for (int kk = 0; kk < CPT; ++kk) {
+            const int c = kk * TPR + lane;
+            if (valid && c < nchunk) {
+                float2 yv[H2], gv[H2], dv[H2];
+                unpack2<T>(yr[kk], yv);
+                unpack2<T>(gr[kk], gv);
+#pragma unroll
+                for (int h = 0; h < H2; ++h) {
+                    const float2 t = __fmul2_rn(yv[h], __fadd2_rn(gv[h], f2(-s)));
+                    dv[h].x = (vis[kk] >> (2 * h)) & 1u ? t.x : 0.f;
+                    dv[h].y = (vis[kk] >> (2 * h + 1)) & 1u ? t.y : 0.f;
+                }
+                st_stream16(dinp + off + c * V, pack2<T>(dv));
+            }
+        }
+        if (valid) pos.next(rows_per_batch, Tq);
+    }
+}
+
+// Looped masked backward (scalar accesses; long, ragged or unaligned rows).
+template <typename T, int TPR>
+__global__ void __launch_bounds__(TPR <= 32 ? 256 : TPR)
+softmax_bw_masked_loop(T *dinp, const T *dout, const T *y, const T *mask, int64_t rows,
+                       int64_t rows_per_batch, int64_t Tq, int64_t Tk, int causal,
+                       int64_t qoff) {
+    pdl_begin();
+    using Tr = Traits<T>;
+    constexpr int BLOCK = TPR <= 32 ? 256 : TPR;
+    constexpr int G = BLOCK / TPR;
+    __shared__ float red[TPR > 32 ? 64 : 1];
+    const int lane = threadIdx.x % TPR;
+    const int grp = threadIdx.x / TPR;
+
+    for (int64_t base = (int64_t)blockIdx.x * G; base < rows;
+         base += (int64_t)gridDim.x * G) {
+        const int64_t row = base + grp;
+        const bool valid = row < rows;
+        const int64_t off = row * Tk;
+        const int64_t qi = causal ? (valid ? row % Tq + qoff : 0) : Tk;
+        const int64_t jend = valid ? (qi < Tk ? qi + 1 : Tk) : 0;
+        const T *mrow = (valid && mask) ? mask + (row / rows_per_batch) * Tk : nullptr;
+        float s = 0.f;
+        for (int64_t j = lane; j < jend; j += TPR) {
+            if (mrow && Tr::load1_cached(mrow + j) == -INFINITY) continue;
+            s += __fmul_rn(Tr::load1(y + off + j), Tr::load1(dout + off + j));
+        }
+        s = group_reduce<TPR, OpSum>(s, red);
+        if (valid)
+            for (int64_t j = lane; j < Tk; j += TPR) {
+                float d = 0.f;
+                if (j < jend && !(mrow && Tr::load1_cached(mrow + j) == -INFINITY))
+                    d = Tr::load1(y + off + j) * (Tr::load1(dout + off + j) - s);
+                Tr::store1(dinp + off + j, d);
             }
     }
 }

@@ -3,7 +3,7 @@
     python -m transformer_reduce_gb300.profile_kernel KERNEL [--workload W] [--launches N]
     python -m transformer_reduce_gb300.profile_kernel --sweep [--launches N]
 
-KERNEL is softmax_fw, softmax_bw, ln_fw, ln_dinp or ln_dgdb.  Only the
+KERNEL is softmax_fw, softmax_bw, softmax_bw_masked, ln_fw, ln_dinp or ln_dgdb.  Only the
 buffers that kernel touches are allocated (for the encoder workload at most
 ~0.8 GB), so a multi-pass ncu capture, which saves and restores device memory
 between passes, stays small while the tensors still exceed L2.
@@ -58,7 +58,13 @@ def prepare(kernel: str, case, dev):
                                                s.causal, _DT[s.dtype], st)), nbytes, keep
         yf = workloads.softmax_probability_like(s, inp["lengths"], device=dev)
         dx = torch.empty_like(x)
-        keep = (dout, yf, dx)
+        keep = (dout, yf, dx, mask)
+        if kernel == "softmax_bw_masked":
+            nbytes = traffic.softmax_bw_masked_bytes(s.B, s.H, s.T, inp["lengths"], s.causal,
+                                                     s.dtype, mask is not None)
+            return (lambda: _lib.ls_softmax_bw_masked(dx.data_ptr(), dout.data_ptr(),
+                                                      yf.data_ptr(), m, s.B, s.H, s.T, s.T,
+                                                      s.causal, _DT[s.dtype], st)), nbytes, keep
         return (lambda: _lib.ls_softmax_bw(dx.data_ptr(), dout.data_ptr(), yf.data_ptr(), s.B,
                                            s.H, s.T, s.T, _DT[s.dtype], st)), \
             traffic.softmax_bw_bytes(s.B, s.H, s.T, s.dtype), keep
@@ -113,7 +119,8 @@ def time_kernel(call, launches: int, dev) -> list:
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("kernel", nargs="?",
-                    choices=["softmax_fw", "softmax_bw", "ln_fw", "ln_dinp", "ln_dgdb"])
+                    choices=["softmax_fw", "softmax_bw", "softmax_bw_masked", "ln_fw", "ln_dinp",
+                             "ln_dgdb"])
     ap.add_argument("--workload", default="encoder_big",
                     help="softmax or LayerNorm case name (encoder_big picks the encoder's case)")
     ap.add_argument("--launches", type=int, default=3)
@@ -129,7 +136,8 @@ def main(argv=None):
             peak = json.load(open(os.path.join(root, "MEASURED_PEAKS.json")))["hbm_gbs"]
         except Exception:
             pass
-        jobs = [(k, c) for k in ("softmax_fw", "softmax_bw") for c in SOFTMAX_CASES.values()]
+        jobs = [(k, c) for k in ("softmax_fw", "softmax_bw", "softmax_bw_masked")
+                for c in SOFTMAX_CASES.values()]
         jobs += [(k, c) for k in ("ln_fw", "ln_dinp", "ln_dgdb") for c in LN_CASES.values()]
         for kernel, case in jobs:
             call, nbytes, keep = prepare(kernel, case, dev)

@@ -6,6 +6,7 @@ fp32.
 Per row (Tk keys, N features):
   softmax fw : reads the v visible keys (v = unmasked, non-future), writes Tk
   softmax bw : reads out_fw and dout (2 Tk), writes dinp (Tk)
+  softmax bw, masked : reads out_fw and dout on the v visible keys (2 v), writes Tk
   LN fw      : reads x (N), writes y (N) and mean, rstd (8 bytes)
   LN dinp    : reads dy, x (2N) and mean, rstd, writes dx (N)
   LN dg/db   : reads dy, x (2N) and mean, rstd
@@ -51,6 +52,14 @@ def softmax_bw_out_fw_read_bytes(B, H, T, dtype) -> int:
 
 def softmax_bw_bytes(B, H, T, dtype) -> int:
     return 3 * B * H * T * T * ELEM_BYTES[dtype]
+
+
+def softmax_bw_masked_bytes(B, H, T, lengths, causal, dtype, has_mask=True) -> int:
+    s = ELEM_BYTES[dtype]
+    reads = 2 * visible_keys(T, lengths, causal, H) * s
+    writes = B * H * T * T * s
+    mask = B * T * s if has_mask else 0
+    return reads + writes + mask
 
 
 def layernorm_fw_bytes(rows, N, dtype) -> int:
