@@ -82,6 +82,12 @@ def _load():
         lib.ref_layernorm_bw_dgamma_dbeta.argtypes = [dp, dp, dp, dp, dp, dp,
                                                       i64, i64]
         lib.ref_layernorm_bw_dgamma_dbeta.restype = None
+        lib.ref_rmsnorm_fw.argtypes = [dp, dp, dp, dp, i64, i64, ctypes.c_double]
+        lib.ref_rmsnorm_fw.restype = None
+        lib.ref_rmsnorm_bw_dinp.argtypes = [dp, dp, dp, dp, dp, i64, i64]
+        lib.ref_rmsnorm_bw_dinp.restype = None
+        lib.ref_rmsnorm_bw_dgamma.argtypes = [dp, dp, dp, dp, i64, i64]
+        lib.ref_rmsnorm_bw_dgamma.restype = None
         _lib = lib
         return lib
 
@@ -256,3 +262,34 @@ def layernorm_bw_dgamma_dbeta(dy, x, mean, rstd):
     _load().ref_layernorm_bw_dgamma_dbeta(_ptr(dgamma), _ptr(dbeta), _ptr(dy),
                                           _ptr(x), _ptr(mean), _ptr(rstd), rows, n)
     return dgamma, dbeta
+
+
+def rmsnorm_fw(x, gamma, eps):
+    """RMSNorm: y = x * rsqrt(mean(x^2) + eps) * gamma; returns (y, rstd) float64."""
+    x, gamma = _f64(x), _f64(gamma)
+    rows, n = x.shape
+    assert gamma.shape == (n,)
+    y = np.empty_like(x)
+    rstd = np.empty(rows)
+    _load().ref_rmsnorm_fw(_ptr(y), _ptr(rstd), _ptr(x), _ptr(gamma), rows, n, float(eps))
+    return y, rstd
+
+
+def rmsnorm_bw_dinp(dy, x, gamma, rstd):
+    """Input gradient of RMSNorm given the saved rstd."""
+    dy, x, gamma, rstd = map(_f64, (dy, x, gamma, rstd))
+    rows, n = x.shape
+    assert dy.shape == x.shape and gamma.shape == (n,) and rstd.shape == (rows,)
+    dx = np.empty_like(x)
+    _load().ref_rmsnorm_bw_dinp(_ptr(dx), _ptr(dy), _ptr(x), _ptr(gamma), _ptr(rstd), rows, n)
+    return dx
+
+
+def rmsnorm_bw_dgamma(dy, x, rstd):
+    """gamma gradient of RMSNorm: column sums of dy * x * rstd."""
+    dy, x, rstd = map(_f64, (dy, x, rstd))
+    rows, n = x.shape
+    assert dy.shape == x.shape and rstd.shape == (rows,)
+    dg = np.empty(n)
+    _load().ref_rmsnorm_bw_dgamma(_ptr(dg), _ptr(dy), _ptr(x), _ptr(rstd), rows, n)
+    return dg

@@ -33,6 +33,10 @@
  *     mu(x^2) - mu(x)^2 implies, and eps sits inside the square root;
  *   - scores are finite (a masked key contributes exp(-inf) = 0).
  *
+ *   [FT]  "FastTransformer: Breaking the Compiler Ceiling via Architectural
+ *         Co-Design", section 5.4 "Vectorized Pre-RMSNorm": RMSNorm, the
+ *         LayerNorm without mean centring (scale only, no bias).
+ *
  * Functions take row-major double arrays; the Python wrapper in this package
  * converts the storage-dtype inputs exactly (every fp32/fp16/bf16 value is a
  * double) and rounds nothing on the way in.
@@ -344,5 +348,71 @@ void ref_layernorm_bw_dgamma_dbeta(double *dgamma, double *dbeta,
         }
         dgamma[j] = dg;
         dbeta[j] = db;
+    }
+}
+
+/* ------------------------------------------------------------------------ */
+/* RMSNorm ([FT] section 5.4)                                                */
+/* ------------------------------------------------------------------------ */
+/*
+ * Per row of x [rows, N]:
+ *   ms   = (1/N) sum_j x_j^2
+ *   rstd = 1 / sqrt(ms + eps)
+ *   y_j  = x_j * rstd * gamma_j
+ * y, x : [rows, N];  gamma : [N];  rstd : [rows]
+ */
+void ref_rmsnorm_fw(double *y, double *rstd, const double *x, const double *gamma,
+                    int64_t rows, int64_t N, double eps)
+{
+    for (int64_t r = 0; r < rows; ++r) {
+        const double *xr = x + r * N;
+        double *yr = y + r * N;
+        double ms = 0.0;
+        for (int64_t j = 0; j < N; ++j)
+            ms += xr[j] * xr[j];
+        ms /= (double)N;
+        double rs = 1.0 / sqrt(ms + eps);
+        for (int64_t j = 0; j < N; ++j)
+            yr[j] = xr[j] * rs * gamma[j];
+        rstd[r] = rs;
+    }
+}
+
+/*
+ * Input gradient of y = x * rstd * gamma, rstd = (mean(x^2) + eps)^(-1/2),
+ * given the saved rstd:
+ *   xhat_j = x_j * rstd,   g_j = gamma_j * dy_j
+ *   dx_j   = rstd * ( g_j - xhat_j * (1/N) sum_k g_k xhat_k )
+ * (d rstd / d x_j = -rstd^3 x_j / N; the single sum is the RMSNorm analogue
+ * of the two LayerNorm sums.)
+ */
+void ref_rmsnorm_bw_dinp(double *dx, const double *dy, const double *x,
+                         const double *gamma, const double *rstd, int64_t rows, int64_t N)
+{
+    for (int64_t r = 0; r < rows; ++r) {
+        const double *xr = x + r * N;
+        const double *dyr = dy + r * N;
+        double *dxr = dx + r * N;
+        double sum_gx = 0.0;
+        for (int64_t k = 0; k < N; ++k)
+            sum_gx += gamma[k] * dyr[k] * (xr[k] * rstd[r]);
+        double b = sum_gx / (double)N;
+        for (int64_t j = 0; j < N; ++j) {
+            double xhat = xr[j] * rstd[r];
+            double g = gamma[j] * dyr[j];
+            dxr[j] = rstd[r] * (g - xhat * b);
+        }
+    }
+}
+
+/* dgamma_j = sum_r dy_rj * x_rj * rstd_r  (column sums in row order). */
+void ref_rmsnorm_bw_dgamma(double *dgamma, const double *dy, const double *x,
+                           const double *rstd, int64_t rows, int64_t N)
+{
+    for (int64_t j = 0; j < N; ++j) {
+        double dg = 0.0;
+        for (int64_t r = 0; r < rows; ++r)
+            dg += dy[r * N + j] * (x[r * N + j] * rstd[r]);
+        dgamma[j] = dg;
     }
 }

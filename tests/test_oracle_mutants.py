@@ -45,6 +45,12 @@ MUTANTS = [
     ("visible_offset_dropped", "if (causal && j > q + offset)\n        return 0;",
      "if (causal && j > q)\n        return 0;", 0),
     ("fw_offset_dropped", "if (causal && j > q + offset)", "if (causal && j > q)", 1),
+    ("rms_no_square", "ms += xr[j] * xr[j];", "ms += xr[j];", 0),
+    ("rms_eps_outside", "double rs = 1.0 / sqrt(ms + eps);", "double rs = 1.0 / (sqrt(ms) + eps);", 0),
+    ("rms_mean_subtracted", "yr[j] = xr[j] * rs * gamma[j];", "yr[j] = (xr[j] - ms) * rs * gamma[j];", 0),
+    ("rms_bw_drop_term", "dxr[j] = rstd[r] * (g - xhat * b);", "dxr[j] = rstd[r] * g;", 0),
+    ("rms_bw_sign", "dxr[j] = rstd[r] * (g - xhat * b);", "dxr[j] = rstd[r] * (g + xhat * b);", 0),
+    ("rms_dgamma_no_rstd", "dg += dy[r * N + j] * (x[r * N + j] * rstd[r]);", "dg += dy[r * N + j] * x[r * N + j];", 0),
     ("masked_bw_sum_all_keys", "if (visible(mr, k, q, offset, causal))\n                s += yr[k] * dyr[k];",
      "s += yr[k] * dyr[k];", 0),
     ("masked_bw_no_zeroing", "dxr[j] = visible(mr, j, q, offset, causal) ? yr[j] * (dyr[j] - s) : 0.0;",

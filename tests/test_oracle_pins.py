@@ -409,3 +409,78 @@ def test_softmax_bw_masked_ignores_invisible_inputs(ref):
     assert np.all(dx[invisible] == 0.0)
     np.testing.assert_allclose(dx, ref.softmax_bw(dy.reshape(-1, Tk), y.reshape(-1, Tk)).reshape(y.shape),
                                rtol=1e-13, atol=1e-16)
+
+
+# ----------------------------------------------------------------------------
+# RMSNorm (FastTransformer page, section 5.4)
+# ----------------------------------------------------------------------------
+
+def test_rmsnorm_fw_matches_torch(ref):
+    rng = np.random.default_rng(71)
+    x = rng.normal(1, 2, size=(11, 40))
+    g = rng.uniform(0.5, 1.5, size=40)
+    for eps in (1e-6, 0.5):   # a large eps shows where it enters
+        y, rstd = ref.rmsnorm_fw(x, g, eps)
+        want = torch.nn.functional.rms_norm(torch.tensor(x), (40,), torch.tensor(g), eps)
+        np.testing.assert_allclose(y, want.numpy(), rtol=1e-13, atol=1e-14)
+        np.testing.assert_allclose(rstd, 1 / np.sqrt((x * x).mean(axis=1) + eps), rtol=1e-14)
+
+
+def test_rmsnorm_fw_closed_forms(ref):
+    # a constant row c: y = c / sqrt(c^2 + eps) * gamma; with gamma = 1 the
+    # output's mean square is ms / (ms + eps)
+    x = np.full((1, 16), -2.5)
+    g = np.linspace(0.5, 1.5, 16)
+    y, rstd = ref.rmsnorm_fw(x, g, 1e-6)
+    np.testing.assert_allclose(y[0], -2.5 / math.sqrt(6.25 + 1e-6) * g, rtol=1e-15)
+    rng = np.random.default_rng(72)
+    x = rng.normal(0, 3, size=(9, 64))
+    y, rstd = ref.rmsnorm_fw(x, np.ones(64), 1e-3)
+    ms = (x * x).mean(axis=1)
+    np.testing.assert_allclose((y * y).mean(axis=1), ms / (ms + 1e-3), rtol=1e-13)
+    # no mean centring: a shifted row is NOT normalised to the same output
+    y2, _ = ref.rmsnorm_fw(x + 5.0, np.ones(64), 1e-3)
+    assert np.max(np.abs(y2 - y)) > 0.1
+
+
+@pytest.mark.parametrize("rows,n", [(3, 5), (4, 9)])
+def test_rmsnorm_bw_central_differences(ref, rows, n):
+    rng = np.random.default_rng(73)
+    x = rng.normal(0.5, 1.5, size=(rows, n))
+    g = rng.uniform(0.5, 1.5, size=n)
+    dy = rng.normal(size=(rows, n))
+    eps = 1e-3
+
+    def loss(xx, gg):
+        return float(np.sum(dy * ref.rmsnorm_fw(xx, gg, eps)[0]))
+
+    _, rstd = ref.rmsnorm_fw(x, g, eps)
+    dx = ref.rmsnorm_bw_dinp(dy, x, g, rstd)
+    dg = ref.rmsnorm_bw_dgamma(dy, x, rstd)
+    h = 1e-6
+    fdx = np.zeros_like(x)
+    for idx in np.ndindex(x.shape):
+        xp, xm = x.copy(), x.copy()
+        xp[idx] += h
+        xm[idx] -= h
+        fdx[idx] = (loss(xp, g) - loss(xm, g)) / (2 * h)
+    assert np.max(np.abs(dx - fdx)) <= 1e-6 * np.max(np.abs(fdx))
+    for j in range(n):
+        gp, gm = g.copy(), g.copy()
+        gp[j] += h
+        gm[j] -= h
+        assert dg[j] == pytest.approx((loss(x, gp) - loss(x, gm)) / (2 * h), rel=1e-6, abs=1e-8)
+
+
+def test_rmsnorm_bw_matches_torch_autograd(ref):
+    rng = np.random.default_rng(74)
+    rows, n = 6, 33
+    x = torch.tensor(rng.normal(1, 2, size=(rows, n)), requires_grad=True)
+    g = torch.tensor(rng.uniform(0.5, 1.5, size=n), requires_grad=True)
+    dy = torch.tensor(rng.normal(size=(rows, n)))
+    torch.nn.functional.rms_norm(x, (n,), g, 1e-6).backward(dy)
+    _, rstd = ref.rmsnorm_fw(x.detach().numpy(), g.detach().numpy(), 1e-6)
+    np.testing.assert_allclose(ref.rmsnorm_bw_dinp(dy.numpy(), x.detach().numpy(), g.detach().numpy(), rstd),
+                               x.grad.numpy(), rtol=1e-11, atol=1e-12)
+    np.testing.assert_allclose(ref.rmsnorm_bw_dgamma(dy.numpy(), x.detach().numpy(), rstd),
+                               g.grad.numpy(), rtol=1e-11, atol=1e-12)
