@@ -243,6 +243,52 @@ ls_status ls_layernorm_bw_dgamma_dbeta_noalloc(float *dgamma, float *dbeta,
                                                int64_t rows, int64_t hidden,
                                                ls_dtype dt, void *stream);
 
+/*
+ * RMSNorm forward: the one-reduction LayerNorm variant of the page
+ * "FastTransformer: Breaking the Compiler Ceiling via Architectural
+ * Co-Design", section 5.4 "Vectorized Pre-RMSNorm" (no mean centring, no
+ * bias).  Per row of x [rows, hidden]:
+ *     rstd = 1 / sqrt(mean(x^2) + eps),   y_j = x_j * rstd * gamma_j
+ *
+ *   y      [rows, hidden] dt, device, written.
+ *   rstd   [rows] float32, device, written (saved for the backward).
+ *   x      [rows, hidden] dt, device, read.
+ *   gamma  [hidden] dt, device, read.
+ *   eps    added inside the square root (the page uses 1e-6).
+ * Errors as for ls_layernorm_fw.
+ */
+ls_status ls_rmsnorm_fw(void *y, float *rstd, const void *x, const void *gamma, int64_t rows,
+                        int64_t hidden, float eps, ls_dtype dt, void *stream);
+
+/*
+ * RMSNorm backward, input gradient.  With xhat = x * rstd and g = gamma * dy,
+ * per row:  S = sum_j g_j * xhat_j,  dx_j = rstd * (g_j - xhat_j * S / hidden).
+ *
+ *   dx     [rows, hidden] dt, device, written.  May equal `dy`.
+ *   dy, x  [rows, hidden] dt, device, read.
+ *   gamma  [hidden] dt, device, read.
+ *   rstd   [rows] float32, device, read (as saved by ls_rmsnorm_fw).
+ * Errors as for ls_layernorm_bw_dinp.
+ */
+ls_status ls_rmsnorm_bw_dinp(void *dx, const void *dy, const void *x, const void *gamma,
+                             const float *rstd, int64_t rows, int64_t hidden, ls_dtype dt,
+                             void *stream);
+
+/*
+ * RMSNorm backward, gamma gradient: dgamma_j = sum_r dy_rj * x_rj * rstd_r,
+ * in the same fixed order as ls_layernorm_bw_dgamma_dbeta (bitwise
+ * reproducible).  `workspace` as for that function, sized by
+ * ls_layernorm_bw_dgamma_dbeta_workspace_size(rows, hidden).
+ *
+ *   dgamma  [hidden] float32, device, written (overwritten).
+ *   dy, x   [rows, hidden] dt, device, read.
+ *   rstd    [rows] float32, device, read.
+ * Errors as for ls_layernorm_bw_dgamma_dbeta.
+ */
+ls_status ls_rmsnorm_bw_dgamma(float *dgamma, const void *dy, const void *x, const float *rstd,
+                               int64_t rows, int64_t hidden, void *workspace,
+                               size_t workspace_bytes, ls_dtype dt, void *stream);
+
 /* Static, human-readable name of a status code (never NULL). */
 const char *ls_status_string(ls_status s);
 

@@ -89,6 +89,13 @@ def test_rejections_before_launch(abi):
     assert abi.ls_layernorm_fw(None, None, None, None, None, None, 0, 8, 1e-8, F32) == abi.LS_OK
     assert abi.ls_layernorm_bw_dinp(fake, fake, None, fake, fake, fake, 4, 8, F32) == abi.LS_ERR_INVALID_ARG
     assert abi.ls_layernorm_bw_dinp(None, None, None, None, None, None, 0, 8, F32) == abi.LS_OK
+    # RMSNorm
+    assert abi.ls_rmsnorm_fw(fake, fake, fake, fake, 4, 0, 1e-6, F32) == abi.LS_ERR_INVALID_ARG
+    assert abi.ls_rmsnorm_fw(fake, None, fake, fake, 4, 8, 1e-6, F32) == abi.LS_ERR_INVALID_ARG
+    assert abi.ls_rmsnorm_fw(fake, fake, fake, fake, 4, 8, -1.0, F32) == abi.LS_ERR_INVALID_ARG
+    assert abi.ls_rmsnorm_fw(None, None, None, None, 0, 8, 1e-6, F32) == abi.LS_OK
+    assert abi.ls_rmsnorm_bw_dinp(fake, fake, fake, fake, fake + 2, 4, 8, F32) == abi.LS_ERR_MISALIGNED
+    assert abi.ls_rmsnorm_bw_dgamma(fake, fake, fake, fake, 16384, 1024, None, 0, BF16) == abi.LS_ERR_WORKSPACE
     # gamma / beta gradient: workspace checks
     need = abi.ls_layernorm_bw_dgamma_dbeta_workspace_size(16384, 1024)
     assert need > 0

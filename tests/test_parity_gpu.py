@@ -496,3 +496,76 @@ def test_softmax_bw_masked_encoder_big_sampled():
     want = oracle.softmax_bw_masked(take_rows(inp["dout"], rows), take_rows(y, rows),
                                     inp["mask"].cpu(), batch=rows // (s.H * s.T))
     compare(take_rows(dx, rows), want, s.dtype, "encoder masked bw")
+
+
+# ----------------------------------------------------------------------------
+# RMSNorm (FastTransformer page, section 5.4)
+# ----------------------------------------------------------------------------
+
+def check_rmsnorm(case, full=True, seed=0, eps=1e-6):
+    from transformer_reduce_gb300 import workloads as W
+    L = _L()
+    inp = W.layernorm_inputs(case, device=DEV)
+    x, g, dy = inp["x"], inp["gamma"], inp["dy"]
+    y, rstd = L.rmsnorm_fw(x, g, eps)
+    torch.cuda.synchronize()
+    R, N = x.shape
+    rows = np.arange(R) if full else sample_rows(R, seed=seed)
+    yr, rr = oracle.rmsnorm_fw(take_rows(x, rows), g.cpu(), eps)
+    compare(take_rows(y, rows), yr, case.dtype, f"{case.name} rms y")
+    compare(rstd.cpu()[rows], rr, case.dtype, f"{case.name} rms rstd")
+    # backward inputs: the oracle's rstd of every row, stored as fp32
+    r_all = np.concatenate([oracle.rmsnorm_fw(x[r0:r0 + 2048].cpu(), g.cpu(), eps)[1]
+                            for r0 in range(0, R, 2048)])
+    rstd_in = torch.from_numpy(r_all).float().to(DEV)
+    dx = L.rmsnorm_bw_dinp(dy, x, g, rstd_in)
+    dg = L.rmsnorm_bw_dgamma(dy, x, rstd_in)
+    torch.cuda.synchronize()
+    compare(take_rows(dx, rows), oracle.rmsnorm_bw_dinp(take_rows(dy, rows), take_rows(x, rows),
+                                                        g.cpu(), rstd_in.cpu()[rows]),
+            case.dtype, f"{case.name} rms dx")
+    cols = np.arange(N) if full else np.unique(np.concatenate(
+        [np.arange(min(8, N)), np.arange(max(0, N - 8), N),
+         np.random.default_rng(seed).integers(0, N, size=48)]))
+    ci = torch.from_numpy(cols).to(DEV)
+    want = oracle.rmsnorm_bw_dgamma(dy.index_select(1, ci).cpu(), x.index_select(1, ci).cpu(),
+                                    rstd_in.cpu())
+    compare(dg.cpu()[cols], want, case.dtype, f"{case.name} rms dgamma")
+
+
+@pytest.mark.parametrize("N", [768, 1024, 4096, 8192])
+def test_rmsnorm_width_sweep_bf16(N):
+    from transformer_reduce_gb300 import workloads as W
+    case = [c for c in W.LAYERNORM_SWEEP if c.hidden == N][0]
+    check_rmsnorm(case, full=False, seed=N)
+
+
+def test_rmsnorm_small_configs():
+    from transformer_reduce_gb300 import workloads as W
+    check_rmsnorm(W.TINY["layernorm"], full=True)
+    check_rmsnorm(W.GPT2_SMALL["layernorm"], full=True)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "f16", "bf16"])
+@pytest.mark.parametrize("N", [1, 7, 100, 770, 1536, 20000])
+def test_rmsnorm_odd_widths(dtype, N):
+    check_rmsnorm(_ln_case(21, N, dtype), full=True)
+
+
+def test_rmsnorm_in_place_gradient_and_zero_rows():
+    L = _L()
+    from transformer_reduce_gb300 import workloads as W
+    lc = _ln_case(40, 1024, "bf16")
+    li = W.layernorm_inputs(lc, device=DEV)
+    _, r = oracle.rmsnorm_fw(li["x"].cpu(), li["gamma"].cpu(), 1e-6)
+    rt = torch.from_numpy(r).float().to(DEV)
+    dy = li["dy"].clone()
+    want = oracle.rmsnorm_bw_dinp(dy.cpu(), li["x"].cpu(), li["gamma"].cpu(), rt.cpu())
+    L.rmsnorm_bw_dinp(dy, li["x"], li["gamma"], rt, dx=dy)
+    torch.cuda.synchronize()
+    compare(dy, want, "bf16", "in-place rms dx")
+    xe = torch.empty(0, 64, device=DEV, dtype=torch.bfloat16)
+    dg = L.rmsnorm_bw_dgamma(xe, xe, torch.empty(0, device=DEV),
+                             dgamma=torch.full((64,), 5.0, device=DEV))
+    torch.cuda.synchronize()
+    assert torch.all(dg == 0)

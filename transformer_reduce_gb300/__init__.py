@@ -13,14 +13,17 @@ from __future__ import annotations
 from ._lib import (LS_BF16, LS_ERR_CUDA, LS_ERR_INVALID_ARG, LS_ERR_MISALIGNED,  # noqa: F401
                    LS_ERR_UNSUPPORTED, LS_ERR_WORKSPACE, LS_F16, LS_F32, LS_OK, LsError,
                    ls_layernorm_bw_dgamma_dbeta, ls_layernorm_bw_dgamma_dbeta_workspace_size,
-                   ls_layernorm_bw_dinp, ls_layernorm_fw, ls_softmax_bw, ls_softmax_bw_masked,
+                   ls_layernorm_bw_dinp, ls_layernorm_fw, ls_rmsnorm_bw_dgamma,
+                   ls_rmsnorm_bw_dinp, ls_rmsnorm_fw, ls_softmax_bw, ls_softmax_bw_masked,
                    ls_softmax_fw, load, status_string)
 
 __all__ = [
     "softmax_fw", "softmax_bw", "softmax_bw_masked", "layernorm_fw", "layernorm_bw_dinp",
-    "layernorm_bw_dgamma_dbeta", "dgamma_dbeta_workspace", "LsError", "load",
+    "layernorm_bw_dgamma_dbeta", "dgamma_dbeta_workspace", "rmsnorm_fw", "rmsnorm_bw_dinp",
+    "rmsnorm_bw_dgamma", "LsError", "load",
     "ls_softmax_fw", "ls_softmax_bw", "ls_softmax_bw_masked", "ls_layernorm_fw", "ls_layernorm_bw_dinp",
     "ls_layernorm_bw_dgamma_dbeta", "ls_layernorm_bw_dgamma_dbeta_workspace_size",
+    "ls_rmsnorm_fw", "ls_rmsnorm_bw_dinp", "ls_rmsnorm_bw_dgamma",
 ]
 
 
@@ -156,3 +159,43 @@ def layernorm_bw_dgamma_dbeta(dy, x, mean, rstd, workspace=None, dgamma=None, db
                                      workspace.numel() * workspace.element_size(), ls_dtype(x),
                                      _stream(x)), "ls_layernorm_bw_dgamma_dbeta")
     return dgamma, dbeta
+
+
+def rmsnorm_fw(x, gamma, eps: float = 1e-6, y=None, rstd=None):
+    """RMSNorm of x [rows, hidden]: y = x * rsqrt(mean(x^2) + eps) * gamma;
+    returns (y, rstd), rstd fp32."""
+    torch = _torch()
+    if x.dim() != 2:
+        raise ValueError("x must be [rows, hidden]")
+    rows, hidden = x.shape
+    y = torch.empty_like(x) if y is None else y
+    rstd = torch.empty(rows, device=x.device, dtype=torch.float32) if rstd is None else rstd
+    _dev(x, gamma, y, rstd)
+    _ok(ls_rmsnorm_fw(_ptr(y), _ptr(rstd), _ptr(x), _ptr(gamma), rows, hidden, float(eps),
+                      ls_dtype(x), _stream(x)), "ls_rmsnorm_fw")
+    return y, rstd
+
+
+def rmsnorm_bw_dinp(dy, x, gamma, rstd, dx=None):
+    """Input gradient of RMSNorm from dy, x and the saved fp32 rstd."""
+    torch = _torch()
+    rows, hidden = x.shape
+    dx = torch.empty_like(x) if dx is None else dx
+    _dev(dy, x, gamma, rstd, dx)
+    _ok(ls_rmsnorm_bw_dinp(_ptr(dx), _ptr(dy), _ptr(x), _ptr(gamma), _ptr(rstd), rows, hidden,
+                           ls_dtype(x), _stream(x)), "ls_rmsnorm_bw_dinp")
+    return dx
+
+
+def rmsnorm_bw_dgamma(dy, x, rstd, workspace=None, dgamma=None):
+    """gamma gradient of RMSNorm (fp32 [hidden]), fixed summation order."""
+    torch = _torch()
+    rows, hidden = x.shape
+    if workspace is None:
+        workspace = dgamma_dbeta_workspace(rows, hidden, x.device)
+    dgamma = torch.empty(hidden, device=x.device, dtype=torch.float32) if dgamma is None else dgamma
+    _dev(dy, x, rstd, workspace, dgamma)
+    _ok(ls_rmsnorm_bw_dgamma(_ptr(dgamma), _ptr(dy), _ptr(x), _ptr(rstd), rows, hidden,
+                             _ptr(workspace), workspace.numel() * workspace.element_size(),
+                             ls_dtype(x), _stream(x)), "ls_rmsnorm_bw_dgamma")
+    return dgamma

@@ -261,6 +261,100 @@ ls_status ls_layernorm_bw_dinp(void *dx, const void *dy, const void *x, const vo
     return LS_ERR_UNSUPPORTED;
 }
 
+ls_status ls_rmsnorm_fw(void *y, float *rstd, const void *x, const void *gamma, int64_t rows,
+                        int64_t hidden, float eps, ls_dtype dt, void *stream) {
+    const size_t es = elem_size(dt);
+    ls_status s = ln_check(rows, hidden, es);
+    if (s != LS_OK) return s;
+    if (!(eps >= 0.f) || !std::isfinite(eps)) return LS_ERR_INVALID_ARG;
+    if (rows == 0) return LS_OK;
+    if (!y || !rstd || !x || !gamma) return LS_ERR_INVALID_ARG;
+    if (!aligned(y, es) || !aligned(x, es) || !aligned(gamma, es) || !aligned(rstd, 4))
+        return LS_ERR_MISALIGNED;
+    const bool vec = vec_ok(hidden, es, {y, x, gamma});
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    switch (dt) {
+        case LS_F32:
+            return from_cuda(lsr::launch_rms_fw<float>((float *)y, rstd, (const float *)x,
+                                                       (const float *)gamma, rows, hidden, eps,
+                                                       vec, st));
+        case LS_F16:
+            return from_cuda(lsr::launch_rms_fw<__half>((__half *)y, rstd, (const __half *)x,
+                                                        (const __half *)gamma, rows, hidden, eps,
+                                                        vec, st));
+        case LS_BF16:
+            return from_cuda(lsr::launch_rms_fw<__nv_bfloat16>(
+                (__nv_bfloat16 *)y, rstd, (const __nv_bfloat16 *)x, (const __nv_bfloat16 *)gamma,
+                rows, hidden, eps, vec, st));
+    }
+    return LS_ERR_UNSUPPORTED;
+}
+
+ls_status ls_rmsnorm_bw_dinp(void *dx, const void *dy, const void *x, const void *gamma,
+                             const float *rstd, int64_t rows, int64_t hidden, ls_dtype dt,
+                             void *stream) {
+    const size_t es = elem_size(dt);
+    ls_status s = ln_check(rows, hidden, es);
+    if (s != LS_OK) return s;
+    if (rows == 0) return LS_OK;
+    if (!dx || !dy || !x || !gamma || !rstd) return LS_ERR_INVALID_ARG;
+    if (!aligned(dx, es) || !aligned(dy, es) || !aligned(x, es) || !aligned(gamma, es) ||
+        !aligned(rstd, 4))
+        return LS_ERR_MISALIGNED;
+    const bool vec = vec_ok(hidden, es, {dx, dy, x, gamma});
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    switch (dt) {
+        case LS_F32:
+            return from_cuda(lsr::launch_rms_dinp<float>((float *)dx, (const float *)dy,
+                                                         (const float *)x, (const float *)gamma,
+                                                         rstd, rows, hidden, vec, st));
+        case LS_F16:
+            return from_cuda(lsr::launch_rms_dinp<__half>((__half *)dx, (const __half *)dy,
+                                                          (const __half *)x,
+                                                          (const __half *)gamma, rstd, rows,
+                                                          hidden, vec, st));
+        case LS_BF16:
+            return from_cuda(lsr::launch_rms_dinp<__nv_bfloat16>(
+                (__nv_bfloat16 *)dx, (const __nv_bfloat16 *)dy, (const __nv_bfloat16 *)x,
+                (const __nv_bfloat16 *)gamma, rstd, rows, hidden, vec, st));
+    }
+    return LS_ERR_UNSUPPORTED;
+}
+
+ls_status ls_rmsnorm_bw_dgamma(float *dgamma, const void *dy, const void *x, const float *rstd,
+                               int64_t rows, int64_t hidden, void *workspace,
+                               size_t workspace_bytes, ls_dtype dt, void *stream) {
+    const size_t es = elem_size(dt);
+    ls_status s = ln_check(rows, hidden, es);
+    if (s != LS_OK) return s;
+    if (!dgamma) return LS_ERR_INVALID_ARG;
+    if (rows > 0 && (!dy || !x || !rstd)) return LS_ERR_INVALID_ARG;
+    if (!aligned(dgamma, 4) || (dy && !aligned(dy, es)) || (x && !aligned(x, es)) ||
+        (rstd && !aligned(rstd, 4)))
+        return LS_ERR_MISALIGNED;
+    const size_t need = ls_layernorm_bw_dgamma_dbeta_workspace_size(rows, hidden);
+    if (need > 0 && (!workspace || workspace_bytes < need || !aligned(workspace, 16)))
+        return LS_ERR_WORKSPACE;
+    const bool vec = vec_ok(hidden, es, {dy, x});
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    float *part = static_cast<float *>(workspace);
+    switch (dt) {
+        case LS_F32:
+            return from_cuda(lsr::launch_rms_dgamma<float>(dgamma, (const float *)dy,
+                                                           (const float *)x, rstd, rows, hidden,
+                                                           part, vec, st));
+        case LS_F16:
+            return from_cuda(lsr::launch_rms_dgamma<__half>(dgamma, (const __half *)dy,
+                                                            (const __half *)x, rstd, rows, hidden,
+                                                            part, vec, st));
+        case LS_BF16:
+            return from_cuda(lsr::launch_rms_dgamma<__nv_bfloat16>(
+                dgamma, (const __nv_bfloat16 *)dy, (const __nv_bfloat16 *)x, rstd, rows, hidden,
+                part, vec, st));
+    }
+    return LS_ERR_UNSUPPORTED;
+}
+
 size_t ls_layernorm_bw_dgamma_dbeta_workspace_size(int64_t rows, int64_t hidden) {
     if (rows <= 0 || hidden <= 0) return 0;
     const int64_t nchunks = lsr::dgdb_num_chunks(rows, hidden);

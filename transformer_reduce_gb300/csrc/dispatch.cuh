@@ -225,16 +225,16 @@ cudaError_t launch_softmax_bw_masked(T *dinp, const T *dout, const T *y, const T
 // ----------------------------------------------------------------------------
 // LayerNorm
 // ----------------------------------------------------------------------------
-template <typename T>
-cudaError_t launch_ln_fw(T *y, float *mean, float *rstd, const T *x, const T *gamma,
-                         const T *beta, int64_t rows, int64_t N, float eps, bool vec,
-                         cudaStream_t st) {
+template <typename T, bool RMS>
+cudaError_t launch_norm_fw(T *y, float *mean, float *rstd, const T *x, const T *gamma,
+                           const T *beta, int64_t rows, int64_t N, float eps, bool vec,
+                           cudaStream_t st) {
     constexpr int V = Traits<T>::kVec;
     int tpr = 0, cpt = 0;
     if (vec && pick_bucket_dense(N / V, kLnMaxCpt, kLnMaxTpr, &tpr, &cpt)) {
 #define X(TPR_, CPT_)                                                                     \
     if (tpr == TPR_ && cpt == CPT_)                                                       \
-        return launch_persistent<ln_fw_vec<T, TPR_, CPT_, kLnFwStages>>(                  \
+        return launch_persistent<ln_fw_vec<T, TPR_, CPT_, kLnFwStages, RMS>>(                  \
             block_threads<TPR_>(), ln_smem<TPR_, CPT_, kLnFwStages, 1, 1>(),                \
             ceil_div(rows, rows_per_block<TPR_>()), st, y, mean, rstd, x, gamma, beta, rows,  \
             (int)N, eps);
@@ -242,22 +242,35 @@ cudaError_t launch_ln_fw(T *y, float *mean, float *rstd, const T *x, const T *ga
 #undef X
     }
     if (N <= kLoopWarpRowMax)
-        return launch_persistent<ln_fw_loop<T, 32>>(256, 0, ceil_div(rows, 8), st, y, mean, rstd, x,
+        return launch_persistent<ln_fw_loop<T, 32, RMS>>(256, 0, ceil_div(rows, 8), st, y, mean, rstd, x,
                                                     gamma, beta, rows, N, eps);
-    return launch_persistent<ln_fw_loop<T, 256>>(256, 0, rows, st, y, mean, rstd, x, gamma, beta,
+    return launch_persistent<ln_fw_loop<T, 256, RMS>>(256, 0, rows, st, y, mean, rstd, x, gamma, beta,
                                                  rows, N, eps);
 }
 
 template <typename T>
-cudaError_t launch_ln_dinp(T *dx, const T *dy, const T *x, const T *gamma,
-                           const float *mean, const float *rstd, int64_t rows,
-                           int64_t N, bool vec, cudaStream_t st) {
+cudaError_t launch_ln_fw(T *y, float *mean, float *rstd, const T *x, const T *gamma,
+                         const T *beta, int64_t rows, int64_t N, float eps, bool vec,
+                         cudaStream_t st) {
+    return launch_norm_fw<T, false>(y, mean, rstd, x, gamma, beta, rows, N, eps, vec, st);
+}
+
+template <typename T>
+cudaError_t launch_rms_fw(T *y, float *rstd, const T *x, const T *gamma, int64_t rows, int64_t N,
+                          float eps, bool vec, cudaStream_t st) {
+    return launch_norm_fw<T, true>(y, nullptr, rstd, x, gamma, nullptr, rows, N, eps, vec, st);
+}
+
+template <typename T, bool RMS>
+cudaError_t launch_norm_dinp(T *dx, const T *dy, const T *x, const T *gamma,
+                             const float *mean, const float *rstd, int64_t rows,
+                             int64_t N, bool vec, cudaStream_t st) {
     constexpr int V = Traits<T>::kVec;
     int tpr = 0, cpt = 0;
     if (vec && pick_bucket_dense(N / V, kLnMaxCpt, kLnMaxTpr, &tpr, &cpt)) {
 #define X(TPR_, CPT_)                                                                       \
     if (tpr == TPR_ && cpt == CPT_)                                                         \
-        return launch_persistent<ln_dinp_vec<T, TPR_, CPT_, kLnDinpStages>>(                \
+        return launch_persistent<ln_dinp_vec<T, TPR_, CPT_, kLnDinpStages, RMS>>(                \
             block_threads<TPR_>(), ln_smem<TPR_, CPT_, kLnDinpStages, 2, 2>(),                \
             ceil_div(rows, rows_per_block<TPR_>()), st, dx, dy, x, gamma, mean, rstd, rows,     \
             (int)N);
@@ -265,10 +278,23 @@ cudaError_t launch_ln_dinp(T *dx, const T *dy, const T *x, const T *gamma,
 #undef X
     }
     if (N <= kLoopWarpRowMax)
-        return launch_persistent<ln_dinp_loop<T, 32>>(256, 0, ceil_div(rows, 8), st, dx, dy, x,
+        return launch_persistent<ln_dinp_loop<T, 32, RMS>>(256, 0, ceil_div(rows, 8), st, dx, dy, x,
                                                       gamma, mean, rstd, rows, N);
-    return launch_persistent<ln_dinp_loop<T, 256>>(256, 0, rows, st, dx, dy, x, gamma, mean, rstd,
+    return launch_persistent<ln_dinp_loop<T, 256, RMS>>(256, 0, rows, st, dx, dy, x, gamma, mean, rstd,
                                                    rows, N);
+}
+
+template <typename T>
+cudaError_t launch_ln_dinp(T *dx, const T *dy, const T *x, const T *gamma,
+                           const float *mean, const float *rstd, int64_t rows,
+                           int64_t N, bool vec, cudaStream_t st) {
+    return launch_norm_dinp<T, false>(dx, dy, x, gamma, mean, rstd, rows, N, vec, st);
+}
+
+template <typename T>
+cudaError_t launch_rms_dinp(T *dx, const T *dy, const T *x, const T *gamma, const float *rstd,
+                            int64_t rows, int64_t N, bool vec, cudaStream_t st) {
+    return launch_norm_dinp<T, true>(dx, dy, x, gamma, nullptr, rstd, rows, N, vec, st);
 }
 
 template <typename T>
@@ -297,6 +323,13 @@ cudaError_t launch_ln_dgdb(float *dgamma, float *dbeta, const T *dy, const T *x,
                       (const float *)part, nchunks, N);
 }
 
+// RMSNorm gamma gradient: the LayerNorm column sums with mean 0 and no dbeta.
+template <typename T>
+cudaError_t launch_rms_dgamma(float *dgamma, const T *dy, const T *x, const float *rstd,
+                              int64_t rows, int64_t N, float *part, bool vec, cudaStream_t st) {
+    return launch_ln_dgdb<T>(dgamma, nullptr, dy, x, nullptr, rstd, rows, N, part, vec, st);
+}
+
 #define LSR_INSTANTIATE(T)                                                                      \
     template cudaError_t launch_softmax_fw<T>(T *, const T *, const T *, int64_t, int64_t,     \
                                               int64_t, int64_t, int, int64_t, bool,            \
@@ -314,6 +347,13 @@ cudaError_t launch_ln_dgdb(float *dgamma, float *dbeta, const T *dy, const T *x,
                                            bool, cudaStream_t);                                \
     template cudaError_t launch_ln_dgdb<T>(float *, float *, const T *, const T *,             \
                                            const float *, const float *, int64_t, int64_t,     \
-                                           float *, bool, cudaStream_t);
+                                           float *, bool, cudaStream_t);                       \
+    template cudaError_t launch_rms_fw<T>(T *, float *, const T *, const T *, int64_t, int64_t, \
+                                          float, bool, cudaStream_t);                          \
+    template cudaError_t launch_rms_dinp<T>(T *, const T *, const T *, const T *,              \
+                                            const float *, int64_t, int64_t, bool,             \
+                                            cudaStream_t);                                     \
+    template cudaError_t launch_rms_dgamma<T>(float *, const T *, const T *, const float *,    \
+                                              int64_t, int64_t, float *, bool, cudaStream_t);
 
 }  // namespace lsr

@@ -45,4 +45,15 @@ cudaError_t launch_ln_dgdb(float *dgamma, float *dbeta, const T *dy, const T *x,
                            const float *mean, const float *rstd, int64_t rows,
                            int64_t N, float *part, bool vec, cudaStream_t st);
 
+// RMSNorm (no mean, no beta): forward, input gradient, gamma gradient.
+template <typename T>
+cudaError_t launch_rms_fw(T *y, float *rstd, const T *x, const T *gamma, int64_t rows, int64_t N,
+                          float eps, bool vec, cudaStream_t st);
+template <typename T>
+cudaError_t launch_rms_dinp(T *dx, const T *dy, const T *x, const T *gamma, const float *rstd,
+                            int64_t rows, int64_t N, bool vec, cudaStream_t st);
+template <typename T>
+cudaError_t launch_rms_dgamma(float *dgamma, const T *dy, const T *x, const float *rstd,
+                              int64_t rows, int64_t N, float *part, bool vec, cudaStream_t st);
+
 }  // namespace lsr

@@ -55,9 +55,12 @@ constexpr size_t ln_smem() {
 // shared memory S-1 rows ahead with per-thread cp.async copies (each thread
 // reads back only its own chunks), so the loads of several rows are in
 // flight while one is reduced.  A thread's columns are the same for every
-// row: its gamma/beta chunks are loaded once.  Arithmetic is packed FP32x2.
+// row: its gamma/beta chunks are loaded once.
 // ----------------------------------------------------------------------------
-template <typename T, int TPR, int CPT, int S>
+// RMS = true is RMSNorm (the FastTransformer page, section 5.4): no shift and
+// no mean, one sum of squares, y = x * rstd * gamma; `mean` and `beta` are
+// unused.
+template <typename T, int TPR, int CPT, int S, bool RMS>
 __global__ void __launch_bounds__(TPR <= 32 ? 256 : TPR, (row_kernel_min_blocks<TPR, CPT>()))
 ln_fw_vec(T *y, float *mean, float *rstd, const T *x, const T *gamma,
           const T *beta, int64_t rows, int N, float eps) {
@@ -81,7 +84,6 @@ ln_fw_vec(T *y, float *mean, float *rstd, const T *x, const T *gamma,
     const int64_t per = (rows + ngroups - 1) / ngroups;
     const int64_t rbeg = ((int64_t)blockIdx.x * G + grp) * per;
     const int64_t rend = rbeg + per < rows ? rbeg + per : rows;
-    const uint64_t pol = l2_evict_first_policy();
 
     uint4 gr[CPT], br[CPT];
 #pragma unroll
@@ -89,7 +91,7 @@ ln_fw_vec(T *y, float *mean, float *rstd, const T *x, const T *gamma,
         const int c = k * TPR + lane;
         if (c < nchunk) {
             gr[k] = ld_cached16(gamma + c * V);
-            br[k] = ld_cached16(beta + c * V);
+            if constexpr (!RMS) br[k] = ld_cached16(beta + c * V);
         }
     }
     int64_t inext = rbeg;
@@ -99,9 +101,9 @@ ln_fw_vec(T *y, float *mean, float *rstd, const T *x, const T *gamma,
 #pragma unroll
             for (int k = 0; k < CPT; ++k) {
                 const int c = k * TPR + lane;
-                if (c < nchunk) cp_async16(&stage[(s * CPT + k) * BLOCK + tid], xrow + c * V, pol);
+                if (c < nchunk) cp_async16(&stage[(s * CPT + k) * BLOCK + tid], xrow + c * V);
             }
-            cp_async4(&x0b[s * BLOCK + tid], xrow);
+            if constexpr (!RMS) cp_async4(&x0b[s * BLOCK + tid], xrow);
         }
         ++inext;
         cp_async_commit();
@@ -117,7 +119,7 @@ ln_fw_vec(T *y, float *mean, float *rstd, const T *x, const T *gamma,
 
         const int64_t row = rbeg + k;
         const bool valid = row < rend;
-        const float x0 = valid ? first_elem<T>(x0b[s_cur * BLOCK + tid]) : 0.f;
+        const float x0 = (valid && !RMS) ? first_elem<T>(x0b[s_cur * BLOCK + tid]) : 0.f;
         float2 d[CPT][H2];
         float2 s1 = f2(0.f), s2 = f2(0.f);
 #pragma unroll
@@ -127,36 +129,51 @@ ln_fw_vec(T *y, float *mean, float *rstd, const T *x, const T *gamma,
                 unpack2<T>(stage[(s_cur * CPT + kk) * BLOCK + tid], d[kk]);
 #pragma unroll
                 for (int h = 0; h < H2; ++h) {
-                    d[kk][h] = __fadd2_rn(d[kk][h], f2(-x0));
-                    s1 = __fadd2_rn(s1, d[kk][h]);
-                    s2 = __ffma2_rn(d[kk][h], d[kk][h], s2);
+                    if constexpr (!RMS) {
+                        d[kk][h] = add2(d[kk][h], f2(-x0));
+                        s1 = add2(s1, d[kk][h]);
+                    }
+                    s2 = fma2(d[kk][h], d[kk][h], s2);
                 }
             }
         }
-        float a1 = s1.x + s1.y, a2 = s2.x + s2.y;
-        group_sum2<TPR>(a1, a2, red);
-        const float m1 = a1 * invN;
-        const float var = fmaxf(a2 * invN - m1 * m1, 0.f);
-        const float rs = rsqrtf(var + eps);
+        float m1 = 0.f, rs;
+        if constexpr (RMS) {
+            const float a2 = group_reduce<TPR, OpSum>(s2.x + s2.y, red);
+            rs = rsqrtf(a2 * invN + eps);
+        } else {
+            float a1 = s1.x + s1.y, a2 = s2.x + s2.y;
+            group_sum2<TPR>(a1, a2, red);
+            m1 = a1 * invN;
+            const float var = fmaxf(a2 * invN - m1 * m1, 0.f);
+            rs = rsqrtf(var + eps);
+        }
 
         T *yrow = y + row * (int64_t)N;
 #pragma unroll
         for (int kk = 0; kk < CPT; ++kk) {
             const int c = kk * TPR + lane;
             if (valid && c < nchunk) {
-                float2 gv[H2], bv[H2], yv[H2];
+                float2 gv[H2], yv[H2];
                 unpack2<T>(gr[kk], gv);
-                unpack2<T>(br[kk], bv);
+                if constexpr (RMS) {
 #pragma unroll
-                for (int h = 0; h < H2; ++h) {
-                    const float2 t = __fmul2_rn(__fadd2_rn(d[kk][h], f2(-m1)), f2(rs));
-                    yv[h] = __ffma2_rn(t, gv[h], bv[h]);
+                    for (int h = 0; h < H2; ++h)
+                        yv[h] = mul2(mul2(d[kk][h], f2(rs)), gv[h]);
+                } else {
+                    float2 bv[H2];
+                    unpack2<T>(br[kk], bv);
+#pragma unroll
+                    for (int h = 0; h < H2; ++h) {
+                        const float2 t = mul2(add2(d[kk][h], f2(-m1)), f2(rs));
+                        yv[h] = fma2(t, gv[h], bv[h]);
+                    }
                 }
                 st_stream16(yrow + c * V, pack2<T>(yv));
             }
         }
         if (valid && lane == 0) {
-            mean[row] = x0 + m1;
+            if constexpr (!RMS) mean[row] = x0 + m1;
             rstd[row] = rs;
         }
         s_cur = s_cur + 1 == S ? 0 : s_cur + 1;
@@ -168,7 +185,9 @@ ln_fw_vec(T *y, float *mean, float *rstd, const T *x, const T *gamma,
 // S2 = sum g*xhat in one fused reduction; then dx = rstd*(g - S1/N - xhat*S2/N).
 // Same staging as the forward (dy, x and the row's mean / rstd per stage).
 // ----------------------------------------------------------------------------
-template <typename T, int TPR, int CPT, int S>
+// RMS = true is the RMSNorm input gradient: xhat = x * rstd, one sum
+// S2 = sum g*xhat, dx = rstd * (g - xhat * S2/N); `mean` is unused.
+template <typename T, int TPR, int CPT, int S, bool RMS>
 __global__ void __launch_bounds__(TPR <= 32 ? 256 : TPR, (row_kernel_min_blocks<TPR, CPT>()))
 ln_dinp_vec(T *dx, const T *dy, const T *x, const T *gamma, const float *mean,
             const float *rstd, int64_t rows, int N) {
@@ -192,7 +211,6 @@ ln_dinp_vec(T *dx, const T *dy, const T *x, const T *gamma, const float *mean,
     const int64_t per = (rows + ngroups - 1) / ngroups;
     const int64_t rbeg = ((int64_t)blockIdx.x * G + grp) * per;
     const int64_t rend = rbeg + per < rows ? rbeg + per : rows;
-    const uint64_t pol = l2_evict_first_policy();
 
     uint4 gr[CPT];
 #pragma unroll
@@ -208,11 +226,11 @@ ln_dinp_vec(T *dx, const T *dy, const T *x, const T *gamma, const float *mean,
             for (int k = 0; k < CPT; ++k) {
                 const int c = k * TPR + lane;
                 if (c < nchunk) {
-                    cp_async16(&stage[((s * 2 + 0) * CPT + k) * BLOCK + tid], dy + off + c * V, pol);
-                    cp_async16(&stage[((s * 2 + 1) * CPT + k) * BLOCK + tid], x + off + c * V, pol);
+                    cp_async16(&stage[((s * 2 + 0) * CPT + k) * BLOCK + tid], dy + off + c * V);
+                    cp_async16(&stage[((s * 2 + 1) * CPT + k) * BLOCK + tid], x + off + c * V);
                 }
             }
-            cp_async4(&stat[(s * 2 + 0) * BLOCK + tid], mean + inext);
+            if constexpr (!RMS) cp_async4(&stat[(s * 2 + 0) * BLOCK + tid], mean + inext);
             cp_async4(&stat[(s * 2 + 1) * BLOCK + tid], rstd + inext);
         }
         ++inext;
@@ -229,7 +247,7 @@ ln_dinp_vec(T *dx, const T *dy, const T *x, const T *gamma, const float *mean,
 
         const int64_t row = rbeg + k;
         const bool valid = row < rend;
-        const float mu = valid ? stat[(s_cur * 2 + 0) * BLOCK + tid] : 0.f;
+        const float mu = (valid && !RMS) ? stat[(s_cur * 2 + 0) * BLOCK + tid] : 0.f;
         const float rs = valid ? stat[(s_cur * 2 + 1) * BLOCK + tid] : 0.f;
         float2 g[CPT][H2], xh[CPT][H2];
         float2 s1 = f2(0.f), s2 = f2(0.f);
@@ -245,15 +263,25 @@ ln_dinp_vec(T *dx, const T *dy, const T *x, const T *gamma, const float *mean,
                 for (int h = 0; h < H2; ++h) {
                     // rounded product (never fused into a later add), so that
                     // S1 sums exactly the g the epilogue uses
-                    g[kk][h] = __fmul2_rn(g[kk][h], gv[h]);
-                    xh[kk][h] = __fmul2_rn(__fadd2_rn(xh[kk][h], f2(-mu)), f2(rs));
-                    s1 = __fadd2_rn(s1, g[kk][h]);
-                    s2 = __ffma2_rn(g[kk][h], xh[kk][h], s2);
+                    g[kk][h] = mul2(g[kk][h], gv[h]);
+                    if constexpr (RMS) {
+                        xh[kk][h] = mul2(xh[kk][h], f2(rs));
+                    } else {
+                        xh[kk][h] = mul2(add2(xh[kk][h], f2(-mu)), f2(rs));
+                        s1 = add2(s1, g[kk][h]);
+                    }
+                    s2 = fma2(g[kk][h], xh[kk][h], s2);
                 }
             }
         }
-        float a1 = s1.x + s1.y, a2 = s2.x + s2.y;
-        group_sum2<TPR>(a1, a2, red);
+        float a1 = 0.f, a2;
+        if constexpr (RMS) {
+            a2 = group_reduce<TPR, OpSum>(s2.x + s2.y, red);
+        } else {
+            a1 = s1.x + s1.y;
+            a2 = s2.x + s2.y;
+            group_sum2<TPR>(a1, a2, red);
+        }
         const float2 na = f2(-a1 * invN), nb = f2(-a2 * invN);
         const int64_t off = row * (int64_t)N;
 #pragma unroll
@@ -263,7 +291,7 @@ ln_dinp_vec(T *dx, const T *dy, const T *x, const T *gamma, const float *mean,
                 float2 ov[H2];
 #pragma unroll
                 for (int h = 0; h < H2; ++h)
-                    ov[h] = __fmul2_rn(f2(rs), __ffma2_rn(xh[kk][h], nb, __fadd2_rn(g[kk][h], na)));
+                    ov[h] = mul2(f2(rs), fma2(xh[kk][h], nb, add2(g[kk][h], na)));
                 st_stream16(dx + off + c * V, pack2<T>(ov));
             }
         }
@@ -274,7 +302,7 @@ ln_dinp_vec(T *dx, const T *dy, const T *x, const T *gamma, const float *mean,
 // ----------------------------------------------------------------------------
 // Looped variants (scalar accesses, any alignment, any row length).
 // ----------------------------------------------------------------------------
-template <typename T, int TPR>
+template <typename T, int TPR, bool RMS>
 __global__ void __launch_bounds__(TPR <= 32 ? 256 : TPR)
 ln_fw_loop(T *y, float *mean, float *rstd, const T *x, const T *gamma,
            const T *beta, int64_t rows, int64_t N, float eps) {
@@ -292,7 +320,7 @@ ln_fw_loop(T *y, float *mean, float *rstd, const T *x, const T *gamma,
         const int64_t row = base + grp;
         const bool valid = row < rows;
         const T *xrow = x + row * N;
-        const float x0 = valid ? Tr::load1_cached(xrow) : 0.f;
+        const float x0 = (valid && !RMS) ? Tr::load1_cached(xrow) : 0.f;
         float s1 = 0.f, s2 = 0.f;
         if (valid)
             for (int64_t j = lane; j < N; j += TPR) {
@@ -300,26 +328,35 @@ ln_fw_loop(T *y, float *mean, float *rstd, const T *x, const T *gamma,
                 s1 += d;
                 s2 = fmaf(d, d, s2);
             }
-        group_sum2<TPR>(s1, s2, red);
-        const float m1 = s1 * invN;
-        const float var = fmaxf(s2 * invN - m1 * m1, 0.f);
-        const float rs = rsqrtf(var + eps);
+        float m1 = 0.f, rs;
+        if constexpr (RMS) {
+            s2 = group_reduce<TPR, OpSum>(s2, red);
+            rs = rsqrtf(s2 * invN + eps);
+        } else {
+            group_sum2<TPR>(s1, s2, red);
+            m1 = s1 * invN;
+            const float var = fmaxf(s2 * invN - m1 * m1, 0.f);
+            rs = rsqrtf(var + eps);
+        }
         if (valid) {
             T *yrow = y + row * N;
             for (int64_t j = lane; j < N; j += TPR) {
                 const float d = Tr::load1(xrow + j) - x0;
-                Tr::store1(yrow + j, fmaf((d - m1) * rs, Tr::load1_cached(gamma + j),
-                                          Tr::load1_cached(beta + j)));
+                if constexpr (RMS)
+                    Tr::store1(yrow + j, __fmul_rn(d * rs, Tr::load1_cached(gamma + j)));
+                else
+                    Tr::store1(yrow + j, fmaf((d - m1) * rs, Tr::load1_cached(gamma + j),
+                                              Tr::load1_cached(beta + j)));
             }
             if (lane == 0) {
-                mean[row] = x0 + m1;
+                if constexpr (!RMS) mean[row] = x0 + m1;
                 rstd[row] = rs;
             }
         }
     }
 }
 
-template <typename T, int TPR>
+template <typename T, int TPR, bool RMS>
 __global__ void __launch_bounds__(TPR <= 32 ? 256 : TPR)
 ln_dinp_loop(T *dx, const T *dy, const T *x, const T *gamma, const float *mean,
              const float *rstd, int64_t rows, int64_t N) {
@@ -337,7 +374,7 @@ ln_dinp_loop(T *dx, const T *dy, const T *x, const T *gamma, const float *mean,
         const int64_t row = base + grp;
         const bool valid = row < rows;
         const int64_t off = row * N;
-        const float mu = valid ? __ldg(mean + row) : 0.f;
+        const float mu = (valid && !RMS) ? __ldg(mean + row) : 0.f;
         const float rs = valid ? __ldg(rstd + row) : 0.f;
         float s1 = 0.f, s2 = 0.f;
         if (valid)
@@ -348,7 +385,12 @@ ln_dinp_loop(T *dx, const T *dy, const T *x, const T *gamma, const float *mean,
                 s1 += g;
                 s2 = fmaf(g, xh, s2);
             }
-        group_sum2<TPR>(s1, s2, red);
+        if constexpr (RMS) {
+            s1 = 0.f;
+            s2 = group_reduce<TPR, OpSum>(s2, red);
+        } else {
+            group_sum2<TPR>(s1, s2, red);
+        }
         const float a = s1 * invN, b = s2 * invN;
         if (valid)
             for (int64_t j = lane; j < N; j += TPR) {
@@ -401,7 +443,7 @@ ln_dgdb_partial(float *part, const T *dy, const T *x, const float *mean,
 #pragma unroll
                 for (int u = 0; u < 4; ++u) {
                     const int64_t rr = r + u * kDgdbWarps;
-                    mu[u] = __ldg(mean + rr);
+                    mu[u] = mean ? __ldg(mean + rr) : 0.f;
                     rs[u] = __ldg(rstd + rr);
                     dv[u] = Tr::load1(dy + rr * N + col0);
                     xv[u] = Tr::load1(x + rr * N + col0);
@@ -416,7 +458,7 @@ ln_dgdb_partial(float *part, const T *dy, const T *x, const float *mean,
 #pragma unroll
                 for (int u = 0; u < 4; ++u) {
                     const int64_t rr = r + u * kDgdbWarps;
-                    mu[u] = __ldg(mean + rr);
+                    mu[u] = mean ? __ldg(mean + rr) : 0.f;
                     rs[u] = __ldg(rstd + rr);
                     rdy[u] = ld_stream16(dy + rr * N + col0);
                     rx[u] = ld_stream16(x + rr * N + col0);
@@ -436,7 +478,7 @@ ln_dgdb_partial(float *part, const T *dy, const T *x, const float *mean,
         }
         for (; r < r1; r += kDgdbWarps) {
             float dv[V], xv[V];
-            const float mu = __ldg(mean + r), rs = __ldg(rstd + r);
+            const float mu = mean ? __ldg(mean + r) : 0.f, rs = __ldg(rstd + r);
             if constexpr (V == 1) {
                 dv[0] = Tr::load1(dy + r * N + col0);
                 xv[0] = Tr::load1(x + r * N + col0);
@@ -519,7 +561,7 @@ ln_dgdb_final(float *dgamma, float *dbeta, const float *part, int64_t nchunks, i
             gb += sb[t][tx];
         }
         dgamma[col] = ga;
-        dbeta[col] = gb;
+        if (dbeta) dbeta[col] = gb;
     }
 }
 

@@ -100,9 +100,8 @@ struct Traits<__nv_bfloat16> {
     }
 };
 
-// Two-element views of a 16-byte vector, for the packed FP32x2 arithmetic of
-// sm_100+ (__fadd2_rn / __fmul2_rn / __ffma2_rn: two FP32 lanes per
-// instruction, each rounded like its scalar counterpart).
+// Two-element views of a 16-byte vector (pairs of FP32 values), with the
+// pair arithmetic below.
 template <typename T>
 __device__ __forceinline__ void unpack2(const uint4 &u, float2 (&f)[Traits<T>::kVec / 2]);
 template <>
@@ -148,6 +147,20 @@ __device__ __forceinline__ uint4 pack2<__nv_bfloat16>(const float2 (&f)[4]) {
 }
 __device__ __forceinline__ float2 f2(float a) { return make_float2(a, a); }
 
+// Pair arithmetic, element by element in scalar FP32, each operation rounded
+// to nearest and never contracted into a fused multiply-add (add2, mul2) or
+// fused exactly once (fma2).  Scalar instructions on purpose: every kernel of
+// the library uses only long-established FP32 instructions.
+__device__ __forceinline__ float2 add2(float2 a, float2 b) {
+    return make_float2(__fadd_rn(a.x, b.x), __fadd_rn(a.y, b.y));
+}
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) {
+    return make_float2(__fmul_rn(a.x, b.x), __fmul_rn(a.y, b.y));
+}
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
+    return make_float2(__fmaf_rn(a.x, b.x, c.x), __fmaf_rn(a.y, b.y, c.y));
+}
+
 // ----------------------------------------------------------------------------
 // Programmatic dependent launch (sm_90+).  Every kernel of the library starts
 // by allowing the next kernel in the stream to be scheduled (its blocks can
@@ -169,20 +182,15 @@ __device__ __forceinline__ void pdl_begin() {
 // its own 16-byte chunks into its own shared-memory slots and later reads only
 // those slots, so `cp.async.wait_group` (which waits for the calling thread's
 // own copies and always completes) is the only synchronisation needed: no
-// barrier, no flag, no spin loop.  The L2 policy marks the streamed data
-// evict-first, as the __ldcs loads do.
+// barrier, no flag, no spin loop.  The .cg form caches in L2 only (the
+// streamed rows are not re-read from L1).
 // ----------------------------------------------------------------------------
 __device__ __forceinline__ uint32_t smem_addr(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
-__device__ __forceinline__ uint64_t l2_evict_first_policy() {
-    uint64_t pol;
-    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
-    return pol;
-}
-__device__ __forceinline__ void cp_async16(void *dst, const void *src, uint64_t pol) {
-    asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;"
-                 :: "r"(smem_addr(dst)), "l"(src), "l"(pol) : "memory");
+__device__ __forceinline__ void cp_async16(void *dst, const void *src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;"
+                 :: "r"(smem_addr(dst)), "l"(src) : "memory");
 }
 __device__ __forceinline__ void cp_async4(void *dst, const void *src) {
     asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" :: "r"(smem_addr(dst)), "l"(src)

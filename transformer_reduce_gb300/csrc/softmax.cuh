@@ -150,7 +150,6 @@ softmax_fw_vec(T *out, const T *inp, const T *mask, int64_t rows,
     const int64_t per = (rows + ngroups - 1) / ngroups;  // rows per group (uniform)
     const int64_t rbeg = ((int64_t)blockIdx.x * G + grp) * per;
     const int64_t rend = rbeg + per < rows ? rbeg + per : rows;
-    const uint64_t pol = l2_evict_first_policy();
 
     RowClasses<T, TPR, CPT> classes(mask, Tk, lane);
 
@@ -167,7 +166,7 @@ softmax_fw_vec(T *out, const T *inp, const T *mask, int64_t rows,
             for (int k = 0; k < CPT; ++k) {
                 const int c = k * TPR + lane;
                 if (c < nchunk && ((cls >> (2 * k)) & 3u) != kChunkSkip)
-                    cp_async16(&stage[(s * CPT + k) * BLOCK + tid], xrow + c * V, pol);
+                    cp_async16(&stage[(s * CPT + k) * BLOCK + tid], xrow + c * V);
             }
             ip.next(rows_per_batch, Tq);
         }
@@ -226,11 +225,11 @@ softmax_fw_vec(T *out, const T *inp, const T *mask, int64_t rows,
             if (valid && c < nchunk && cls != kChunkSkip) {
 #pragma unroll
                 for (int h = 0; h < H2; ++h) {
-                    float2 t = __ffma2_rn(v[kk][h], f2(kLog2e), f2(-mL));
+                    float2 t = fma2(v[kk][h], f2(kLog2e), f2(-mL));
                     t.x = fast_exp2(t.x);
                     t.y = fast_exp2(t.y);
                     v[kk][h] = t;
-                    sum2 = __fadd2_rn(sum2, t);
+                    sum2 = add2(sum2, t);
                 }
             }
         }
@@ -246,7 +245,7 @@ softmax_fw_vec(T *out, const T *inp, const T *mask, int64_t rows,
                 float2 yv[H2];
 #pragma unroll
                 for (int h = 0; h < H2; ++h)
-                    yv[h] = cls == kChunkSkip ? f2(0.f) : __fmul2_rn(v[kk][h], inv);
+                    yv[h] = cls == kChunkSkip ? f2(0.f) : mul2(v[kk][h], inv);
                 st_stream16(orow + c * V, pack2<T>(yv));
             }
         }
@@ -478,7 +477,7 @@ softmax_bw_masked_vec(T *dinp, const T *dout, const T *y, const T *mask, int64_t
             unpack2<T>(gr[kk], gv);
 #pragma unroll
             for (int h = 0; h < H2; ++h) {
-                const float2 p = __fmul2_rn(yv[h], gv[h]);
+                const float2 p = mul2(yv[h], gv[h]);
                 s2.x += (vis[kk] >> (2 * h)) & 1u ? p.x : 0.f;
                 s2.y += (vis[kk] >> (2 * h + 1)) & 1u ? p.y : 0.f;
             }
@@ -493,7 +492,7 @@ softmax_bw_masked_vec(T *dinp, const T *dout, const T *y, const T *mask, int64_t
                 unpack2<T>(gr[kk], gv);
 #pragma unroll
                 for (int h = 0; h < H2; ++h) {
-                    const float2 t = __fmul2_rn(yv[h], __fadd2_rn(gv[h], f2(-s)));
+                    const float2 t = mul2(yv[h], add2(gv[h], f2(-s)));
                     dv[h].x = (vis[kk] >> (2 * h)) & 1u ? t.x : 0.f;
                     dv[h].y = (vis[kk] >> (2 * h + 1)) & 1u ? t.y : 0.f;
                 }

@@ -3,7 +3,8 @@
     python -m transformer_reduce_gb300.profile_kernel KERNEL [--workload W] [--launches N]
     python -m transformer_reduce_gb300.profile_kernel --sweep [--launches N]
 
-KERNEL is softmax_fw, softmax_bw, softmax_bw_masked, ln_fw, ln_dinp or ln_dgdb.  Only the
+KERNEL is softmax_fw, softmax_bw, softmax_bw_masked, ln_fw, ln_dinp, ln_dgdb, rms_fw
+or rms_dinp.  Only the
 buffers that kernel touches are allocated (for the encoder workload at most
 ~0.8 GB), so a multi-pass ncu capture, which saves and restores device memory
 between passes, stays small while the tensors still exceed L2.
@@ -80,6 +81,19 @@ def prepare(kernel: str, case, dev):
             y.data_ptr(), mean.data_ptr(), rstd.data_ptr(), li["x"].data_ptr(),
             li["gamma"].data_ptr(), li["beta"].data_ptr(), c.rows, c.hidden, c.eps,
             _DT[c.dtype], st)), traffic.layernorm_fw_bytes(c.rows, c.hidden, c.dtype), keep
+    if kernel == "rms_fw":
+        y = torch.empty_like(li["x"])
+        keep = (li, y, rstd)
+        return (lambda: _lib.ls_rmsnorm_fw(
+            y.data_ptr(), rstd.data_ptr(), li["x"].data_ptr(), li["gamma"].data_ptr(), c.rows,
+            c.hidden, 1e-6, _DT[c.dtype], st)), traffic.rmsnorm_fw_bytes(c.rows, c.hidden, c.dtype), keep
+    if kernel == "rms_dinp":
+        dx = torch.empty_like(li["x"])
+        keep = (li, dx, rstd)
+        return (lambda: _lib.ls_rmsnorm_bw_dinp(
+            dx.data_ptr(), li["dy"].data_ptr(), li["x"].data_ptr(), li["gamma"].data_ptr(),
+            rstd.data_ptr(), c.rows, c.hidden, _DT[c.dtype], st)), \
+            traffic.rmsnorm_dinp_bytes(c.rows, c.hidden, c.dtype), keep
     if kernel == "ln_dinp":
         dx = torch.empty_like(li["x"])
         keep = (li, dx, mean, rstd)
@@ -120,7 +134,7 @@ def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("kernel", nargs="?",
                     choices=["softmax_fw", "softmax_bw", "softmax_bw_masked", "ln_fw", "ln_dinp",
-                             "ln_dgdb"])
+                             "ln_dgdb", "rms_fw", "rms_dinp"])
     ap.add_argument("--workload", default="encoder_big",
                     help="softmax or LayerNorm case name (encoder_big picks the encoder's case)")
     ap.add_argument("--launches", type=int, default=3)
@@ -138,7 +152,8 @@ def main(argv=None):
             pass
         jobs = [(k, c) for k in ("softmax_fw", "softmax_bw", "softmax_bw_masked")
                 for c in SOFTMAX_CASES.values()]
-        jobs += [(k, c) for k in ("ln_fw", "ln_dinp", "ln_dgdb") for c in LN_CASES.values()]
+        jobs += [(k, c) for k in ("ln_fw", "ln_dinp", "ln_dgdb", "rms_fw", "rms_dinp")
+                 for c in LN_CASES.values()]
         for kernel, case in jobs:
             call, nbytes, keep = prepare(kernel, case, dev)
             ms = time_kernel(call, max(a.launches, 5), dev)

@@ -10,6 +10,8 @@ Per row (Tk keys, N features):
   LN fw      : reads x (N), writes y (N) and mean, rstd (8 bytes)
   LN dinp    : reads dy, x (2N) and mean, rstd, writes dx (N)
   LN dg/db   : reads dy, x (2N) and mean, rstd
+  RMS fw     : reads x (N), writes y (N) and rstd (4 bytes)
+  RMS dinp   : reads dy, x (2N) and rstd, writes dx (N)
 plus the per-call operands read once (mask [B, Tk]; gamma, beta [N]) and
 written once (dgamma, dbeta [N] fp32).  The FastTransformer page's figure of
 805 MB per step for writing and re-reading the (B,H,T,T) fp32 probability
@@ -75,3 +77,13 @@ def layernorm_dinp_bytes(rows, N, dtype) -> int:
 def layernorm_dgdb_bytes(rows, N, dtype) -> int:
     s = ELEM_BYTES[dtype]
     return rows * (2 * N * s + 8) + 2 * N * 4
+
+
+def rmsnorm_fw_bytes(rows, N, dtype) -> int:
+    s = ELEM_BYTES[dtype]
+    return rows * (2 * N * s + 4) + N * s
+
+
+def rmsnorm_dinp_bytes(rows, N, dtype) -> int:
+    s = ELEM_BYTES[dtype]
+    return rows * (3 * N * s + 4) + N * s
