@@ -205,6 +205,50 @@ ls_status ls_layernorm_bw_dgamma_dbeta(float *dgamma, float *dbeta,
                                        ls_dtype dt, void *stream);
 
 /*
+ * Bytes of device workspace ls_layernorm_bw needs for a [rows, hidden]
+ * problem (the same for every dtype): 8 * hidden bytes for each of at most
+ * 456 partial sums, or what ls_layernorm_bw_dgamma_dbeta needs when that is
+ * more (the scalar path below).  Returns 0 for rows <= 0 or hidden <= 0.
+ * Host-only; launches nothing.
+ */
+size_t ls_layernorm_bw_workspace_size(int64_t rows, int64_t hidden);
+
+/*
+ * Fused LayerNorm backward: the input gradient of ls_layernorm_bw_dinp and the
+ * gamma / beta gradients of ls_layernorm_bw_dgamma_dbeta from one read of dy
+ * and x ("Problem 2.2" of the HW4 page asks for both halves of the backward;
+ * slide 22 of the L10 page lists the per-row sums).  The rows are cut into
+ * contiguous chunks (at most 456 for rows of one 16-byte vector, 304 for up
+ * to 512 vectors, 152 for wider rows) by a rule that depends only on (rows,
+ * hidden, dt); one thread block per chunk writes dx for its rows and its
+ * chunk's column sums of dy * xhat and dy, and a second kernel adds the
+ * chunks in index order.  dgamma and dbeta are therefore bitwise
+ * reproducible from run to run and GPU to GPU; their rounding, and dx's (the
+ * row sums are split across threads differently), may differ from the
+ * separate kernels' in the last bits.
+ *
+ *   dx             [rows, hidden] dt, device, written.  May equal dy (each
+ *                  row's dy is staged on chip before its dx is written).
+ *   dgamma, dbeta  [hidden] float32, device, written (overwritten).
+ *   dy, x          [rows, hidden] dt, device, read.
+ *   gamma          [hidden] dt, device, read.
+ *   mean, rstd     [rows] float32, device, read (as saved by ls_layernorm_fw).
+ *   workspace      device scratch of at least
+ *                  ls_layernorm_bw_workspace_size(rows, hidden) bytes,
+ *                  16-byte aligned, contents ignored; may be NULL when that
+ *                  size is 0.  Calls that overlap on the GPU must not share it.
+ * Errors as for ls_layernorm_bw_dgamma_dbeta.  Rows wider than 1024 16-byte
+ * vectors (hidden > 8192 for 16-bit storage, > 4096 for fp32), or pointers
+ * or widths that are not 16-byte multiples, run the two separate kernels
+ * instead, with the same results as calling them.
+ */
+ls_status ls_layernorm_bw(void *dx, float *dgamma, float *dbeta, const void *dy,
+                          const void *x, const void *gamma, const float *mean,
+                          const float *rstd, int64_t rows, int64_t hidden,
+                          void *workspace, size_t workspace_bytes, ls_dtype dt,
+                          void *stream);
+
+/*
  * Size of the device array that ls_layernorm_bw_dgamma_dbeta_noalloc uses as
  * scratch (4 MiB).  It covers, for example, [16384, 8192] and [16384, 1024].
  */

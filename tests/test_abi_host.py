@@ -96,6 +96,18 @@ def test_rejections_before_launch(abi):
     assert abi.ls_rmsnorm_fw(None, None, None, None, 0, 8, 1e-6, F32) == abi.LS_OK
     assert abi.ls_rmsnorm_bw_dinp(fake, fake, fake, fake, fake + 2, 4, 8, F32) == abi.LS_ERR_MISALIGNED
     assert abi.ls_rmsnorm_bw_dgamma(fake, fake, fake, fake, 16384, 1024, None, 0, BF16) == abi.LS_ERR_WORKSPACE
+    # fused LayerNorm backward
+    nf = abi.ls_layernorm_bw_workspace_size(16384, 1024)
+    assert abi.ls_layernorm_bw(fake, fake, fake, fake, fake, fake, fake, fake, 16384, 1024,
+                               None, 0, BF16) == abi.LS_ERR_WORKSPACE
+    assert abi.ls_layernorm_bw(fake, fake, fake, fake, fake, fake, fake, fake, 16384, 1024,
+                               fake, nf - 4, BF16) == abi.LS_ERR_WORKSPACE
+    assert abi.ls_layernorm_bw(fake, None, fake, fake, fake, fake, fake, fake, 16384, 1024,
+                               fake, nf, BF16) == abi.LS_ERR_INVALID_ARG
+    assert abi.ls_layernorm_bw(fake, fake, fake, fake, fake, fake, fake, fake + 2, 16384, 1024,
+                               fake, nf, BF16) == abi.LS_ERR_MISALIGNED
+    assert abi.ls_layernorm_bw(fake, fake, fake, fake, fake, fake, fake, fake, 16384, 0,
+                               fake, nf, BF16) == abi.LS_ERR_INVALID_ARG
     # gamma / beta gradient: workspace checks
     need = abi.ls_layernorm_bw_dgamma_dbeta_workspace_size(16384, 1024)
     assert need > 0
@@ -123,6 +135,22 @@ def test_workspace_size_depends_only_on_shape(abi):
         # the chunk partials stay small next to the inputs for large problems
         if rows * hidden >= 1 << 22:
             assert n <= 0.1 * rows * hidden * 2 * 2
+
+
+def test_fused_backward_workspace_size():
+    from transformer_reduce_gb300 import _lib
+    _lib.load()
+    ws = _lib.ls_layernorm_bw_workspace_size
+    assert ws(0, 1024) == 0 and ws(16, 0) == 0
+    for rows, hidden in [(1, 1), (303, 64), (304, 64), (305, 64), (16384, 1024), (7, 20000)]:
+        n = ws(rows, hidden)
+        # one chunk per row up to 456 rows, then at most 456 chunks; one
+        # partial sum per chunk
+        chunks = rows if rows <= 456 else len(range(0, rows, -(-rows // 456)))
+        assert n >= chunks * 2 * 4 * hidden
+        assert n <= max(456 * 2 * 4 * hidden,
+                        _lib.ls_layernorm_bw_dgamma_dbeta_workspace_size(rows, hidden))
+        assert n >= _lib.ls_layernorm_bw_dgamma_dbeta_workspace_size(rows, hidden)
 
 
 def test_byte_model_reproduces_the_pages_figure():

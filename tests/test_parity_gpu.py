@@ -569,3 +569,91 @@ def test_rmsnorm_in_place_gradient_and_zero_rows():
                              dgamma=torch.full((64,), 5.0, device=DEV))
     torch.cuda.synchronize()
     assert torch.all(dg == 0)
+
+
+# ----------------------------------------------------------------------------
+# fused LayerNorm backward: dx, dgamma, dbeta from one read of dy and x
+# ----------------------------------------------------------------------------
+
+def check_ln_bw_fused(case, full=True, seed=0):
+    from transformer_reduce_gb300 import workloads as W
+    L = _L()
+    inp = W.layernorm_inputs(case, device=DEV)
+    x, g, b, dy = inp["x"], inp["gamma"], inp["beta"], inp["dy"]
+    R, N = x.shape
+    m_all, r_all = oracle_ln_stats(x, g, b, case.eps)
+    mean_in = torch.from_numpy(m_all).float().to(DEV)
+    rstd_in = torch.from_numpy(r_all).float().to(DEV)
+    dx, dgm, dbt = L.layernorm_bw(dy, x, g, mean_in, rstd_in)
+    torch.cuda.synchronize()
+    rows = np.arange(R) if full else sample_rows(R, seed=seed)
+    refdx = oracle.layernorm_bw_dinp(take_rows(dy, rows), take_rows(x, rows), g.cpu(),
+                                     mean_in.cpu()[rows], rstd_in.cpu()[rows])
+    compare(take_rows(dx, rows), refdx, case.dtype, f"{case.name} fused dx")
+    cols = np.arange(N) if full else np.unique(np.concatenate(
+        [np.arange(min(8, N)), np.arange(max(0, N - 8), N),
+         np.random.default_rng(seed).integers(0, N, size=48)]))
+    ci = torch.from_numpy(cols).to(DEV)
+    rg, rb = oracle.layernorm_bw_dgamma_dbeta(dy.index_select(1, ci).cpu(),
+                                              x.index_select(1, ci).cpu(),
+                                              mean_in.cpu(), rstd_in.cpu())
+    compare(dgm.cpu()[cols], rg, case.dtype, f"{case.name} fused dgamma")
+    compare(dbt.cpu()[cols], rb, case.dtype, f"{case.name} fused dbeta")
+    return dy, x, g, mean_in, rstd_in, (dx, dgm, dbt)
+
+
+@pytest.mark.parametrize("N", [768, 1024, 4096, 8192])
+def test_ln_bw_fused_width_sweep_bf16(N):
+    from transformer_reduce_gb300 import workloads as W
+    case = [c for c in W.LAYERNORM_SWEEP if c.hidden == N][0]
+    check_ln_bw_fused(case, full=False, seed=N)
+
+
+def test_ln_bw_fused_small_configs_and_encoder():
+    from transformer_reduce_gb300 import workloads as W
+    check_ln_bw_fused(W.TINY["layernorm"], full=True)
+    check_ln_bw_fused(W.GPT2_SMALL["layernorm"], full=True)
+    check_ln_bw_fused(W.ENCODER_BIG["layernorm"][1], full=False, seed=5)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "f16", "bf16"])
+@pytest.mark.parametrize("rows,N", [(1, 64), (7, 1024), (303, 256), (304, 512), (305, 768),
+                                    (1000, 2048), (21, 7), (21, 770), (21, 20000)])
+def test_ln_bw_fused_ragged_chunks_and_widths(dtype, rows, N):
+    # row counts around the 304-chunk cut (one row per chunk, a ragged last
+    # chunk) and widths that take the scalar two-kernel path
+    check_ln_bw_fused(_ln_case(rows, N, dtype), full=True)
+
+
+def test_ln_bw_fused_is_bitwise_reproducible_and_in_place():
+    L = _L()
+    case = _ln_case(4099, 1024, "bf16")
+    dy, x, g, m, r, (dx0, dg0, db0) = check_ln_bw_fused(case, full=False, seed=3)
+    for _ in range(2):
+        dx1, dg1, db1 = L.layernorm_bw(dy, x, g, m, r)
+        torch.cuda.synchronize()
+        assert torch.equal(dx0, dx1) and torch.equal(dg0, dg1) and torch.equal(db0, db1)
+    # dx written over dy
+    d = dy.clone()
+    L.layernorm_bw(d, x, g, m, r, dx=d)
+    torch.cuda.synchronize()
+    assert torch.equal(d, dx0)
+
+
+def test_ln_bw_fused_zero_rows_and_workspace_rejection():
+    L = _L()
+    xe = torch.empty(0, 64, device=DEV, dtype=torch.bfloat16)
+    _, dg, db = L.layernorm_bw(xe, xe, torch.ones(64, device=DEV, dtype=torch.bfloat16),
+                               torch.empty(0, device=DEV), torch.empty(0, device=DEV),
+                               dgamma=torch.full((64,), 7.0, device=DEV),
+                               dbeta=torch.full((64,), 7.0, device=DEV))
+    torch.cuda.synchronize()
+    assert torch.all(dg == 0) and torch.all(db == 0)
+    case = _ln_case(4096, 1024, "bf16")
+    from transformer_reduce_gb300 import workloads as W
+    li = W.layernorm_inputs(case, device=DEV)
+    m = torch.zeros(4096, device=DEV)
+    need = L.ls_layernorm_bw_workspace_size(4096, 1024)
+    small = torch.empty(need // 4 - 1, device=DEV)
+    with pytest.raises(L.LsError):
+        L.layernorm_bw(li["dy"], li["x"], li["gamma"], m, m, workspace=small)

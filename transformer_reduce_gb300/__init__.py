@@ -13,17 +13,18 @@ from __future__ import annotations
 from ._lib import (LS_BF16, LS_ERR_CUDA, LS_ERR_INVALID_ARG, LS_ERR_MISALIGNED,  # noqa: F401
                    LS_ERR_UNSUPPORTED, LS_ERR_WORKSPACE, LS_F16, LS_F32, LS_OK, LsError,
                    ls_layernorm_bw_dgamma_dbeta, ls_layernorm_bw_dgamma_dbeta_workspace_size,
-                   ls_layernorm_bw_dinp, ls_layernorm_fw, ls_rmsnorm_bw_dgamma,
+                   ls_layernorm_bw, ls_layernorm_bw_dinp, ls_layernorm_bw_workspace_size,
+                   ls_layernorm_fw, ls_rmsnorm_bw_dgamma,
                    ls_rmsnorm_bw_dinp, ls_rmsnorm_fw, ls_softmax_bw, ls_softmax_bw_masked,
                    ls_softmax_fw, load, status_string)
 
 __all__ = [
     "softmax_fw", "softmax_bw", "softmax_bw_masked", "layernorm_fw", "layernorm_bw_dinp",
-    "layernorm_bw_dgamma_dbeta", "dgamma_dbeta_workspace", "rmsnorm_fw", "rmsnorm_bw_dinp",
+    "layernorm_bw_dgamma_dbeta", "dgamma_dbeta_workspace", "layernorm_bw", "rmsnorm_fw", "rmsnorm_bw_dinp",
     "rmsnorm_bw_dgamma", "LsError", "load",
     "ls_softmax_fw", "ls_softmax_bw", "ls_softmax_bw_masked", "ls_layernorm_fw", "ls_layernorm_bw_dinp",
     "ls_layernorm_bw_dgamma_dbeta", "ls_layernorm_bw_dgamma_dbeta_workspace_size",
-    "ls_rmsnorm_fw", "ls_rmsnorm_bw_dinp", "ls_rmsnorm_bw_dgamma",
+    "ls_layernorm_bw", "ls_layernorm_bw_workspace_size", "ls_rmsnorm_fw", "ls_rmsnorm_bw_dinp", "ls_rmsnorm_bw_dgamma",
 ]
 
 
@@ -159,6 +160,25 @@ def layernorm_bw_dgamma_dbeta(dy, x, mean, rstd, workspace=None, dgamma=None, db
                                      workspace.numel() * workspace.element_size(), ls_dtype(x),
                                      _stream(x)), "ls_layernorm_bw_dgamma_dbeta")
     return dgamma, dbeta
+
+
+def layernorm_bw(dy, x, gamma, mean, rstd, workspace=None, dx=None, dgamma=None, dbeta=None):
+    """Whole LayerNorm backward in one pass over dy and x: returns
+    (dx, dgamma, dbeta), the parameter gradients fp32 in a fixed order."""
+    torch = _torch()
+    rows, hidden = x.shape
+    if workspace is None:
+        n = ls_layernorm_bw_workspace_size(rows, hidden)
+        workspace = torch.empty(max(n, 16) // 4, device=x.device, dtype=torch.float32)
+    dx = torch.empty_like(x) if dx is None else dx
+    dgamma = torch.empty(hidden, device=x.device, dtype=torch.float32) if dgamma is None else dgamma
+    dbeta = torch.empty(hidden, device=x.device, dtype=torch.float32) if dbeta is None else dbeta
+    _dev(dy, x, gamma, mean, rstd, workspace, dx, dgamma, dbeta)
+    _ok(ls_layernorm_bw(_ptr(dx), _ptr(dgamma), _ptr(dbeta), _ptr(dy), _ptr(x), _ptr(gamma),
+                        _ptr(mean), _ptr(rstd), rows, hidden, _ptr(workspace),
+                        workspace.numel() * workspace.element_size(), ls_dtype(x), _stream(x)),
+        "ls_layernorm_bw")
+    return dx, dgamma, dbeta
 
 
 def rmsnorm_fw(x, gamma, eps: float = 1e-6, y=None, rstd=None):

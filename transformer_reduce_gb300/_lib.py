@@ -34,6 +34,9 @@ SIGNATURES = {
                                      _INT),
     "ls_layernorm_bw_dgamma_dbeta_noalloc": ([_VP, _VP, _VP, _VP, _VP, _VP, _I64, _I64, _INT, _VP],
                                              _INT),
+    "ls_layernorm_bw_workspace_size": ([_I64, _I64], _SZ),
+    "ls_layernorm_bw": ([_VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _I64, _I64, _VP, _SZ, _INT, _VP],
+                        _INT),
     "ls_rmsnorm_fw": ([_VP, _VP, _VP, _VP, _I64, _I64, _F32, _INT, _VP], _INT),
     "ls_rmsnorm_bw_dinp": ([_VP, _VP, _VP, _VP, _VP, _I64, _I64, _INT, _VP], _INT),
     "ls_rmsnorm_bw_dgamma": ([_VP, _VP, _VP, _VP, _I64, _I64, _VP, _SZ, _INT, _VP], _INT),
@@ -111,6 +114,16 @@ def ls_layernorm_bw_dgamma_dbeta_noalloc(dgamma, dbeta, dy, x, mean, rstd, rows,
     header for its size limit and the rule that overlapping calls race)."""
     return load().ls_layernorm_bw_dgamma_dbeta_noalloc(dgamma, dbeta, dy, x, mean, rstd, rows,
                                                        hidden, dt, stream)
+
+
+def ls_layernorm_bw_workspace_size(rows, hidden) -> int:
+    return load().ls_layernorm_bw_workspace_size(rows, hidden)
+
+
+def ls_layernorm_bw(dx, dgamma, dbeta, dy, x, gamma, mean, rstd, rows, hidden, workspace,
+                    workspace_bytes, dt, stream=0) -> int:
+    return load().ls_layernorm_bw(dx, dgamma, dbeta, dy, x, gamma, mean, rstd, rows, hidden,
+                                  workspace, workspace_bytes, dt, stream)
 
 
 def ls_rmsnorm_fw(y, rstd, x, gamma, rows, hidden, eps, dt, stream=0) -> int:

@@ -31,6 +31,14 @@ int64_t dgdb_num_chunks(int64_t rows, int64_t hidden) {
     return (rows + rpc - 1) / rpc;
 }
 
+int64_t ln_bw_fused_max_parts(int64_t rows) {
+    // 456 chunks is the most any bucket uses (fewer chunks of more rows never
+    // need more slots); one slot per chunk
+    if (rows <= 0) return 0;
+    const int64_t rpc = (rows + 455) / 456;
+    return (rows + rpc - 1) / rpc;
+}
+
 int device_sm_count() {
     constexpr int kMaxDev = 64;
     static std::atomic<int> cache[kMaxDev];
@@ -350,6 +358,50 @@ ls_status ls_rmsnorm_bw_dgamma(float *dgamma, const void *dy, const void *x, con
         case LS_BF16:
             return from_cuda(lsr::launch_rms_dgamma<__nv_bfloat16>(
                 dgamma, (const __nv_bfloat16 *)dy, (const __nv_bfloat16 *)x, rstd, rows, hidden,
+                part, vec, st));
+    }
+    return LS_ERR_UNSUPPORTED;
+}
+
+size_t ls_layernorm_bw_workspace_size(int64_t rows, int64_t hidden) {
+    if (rows <= 0 || hidden <= 0) return 0;
+    const size_t fused = (size_t)lsr::ln_bw_fused_max_parts(rows) * 2u * (size_t)hidden * 4u;
+    const size_t split = ls_layernorm_bw_dgamma_dbeta_workspace_size(rows, hidden);
+    return fused > split ? fused : split;
+}
+
+ls_status ls_layernorm_bw(void *dx, float *dgamma, float *dbeta, const void *dy, const void *x,
+                          const void *gamma, const float *mean, const float *rstd, int64_t rows,
+                          int64_t hidden, void *workspace, size_t workspace_bytes, ls_dtype dt,
+                          void *stream) {
+    const size_t es = elem_size(dt);
+    ls_status s = ln_check(rows, hidden, es);
+    if (s != LS_OK) return s;
+    if (!dgamma || !dbeta) return LS_ERR_INVALID_ARG;
+    if (rows > 0 && (!dx || !dy || !x || !gamma || !mean || !rstd)) return LS_ERR_INVALID_ARG;
+    if (!aligned(dgamma, 4) || !aligned(dbeta, 4) || (dx && !aligned(dx, es)) ||
+        (dy && !aligned(dy, es)) || (x && !aligned(x, es)) || (gamma && !aligned(gamma, es)) ||
+        (mean && !aligned(mean, 4)) || (rstd && !aligned(rstd, 4)))
+        return LS_ERR_MISALIGNED;
+    const size_t need = ls_layernorm_bw_workspace_size(rows, hidden);
+    if (need > 0 && (!workspace || workspace_bytes < need || !aligned(workspace, 16)))
+        return LS_ERR_WORKSPACE;
+    const bool vec = vec_ok(hidden, es, {dx, dy, x, gamma});
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    float *part = static_cast<float *>(workspace);
+    switch (dt) {
+        case LS_F32:
+            return from_cuda(lsr::launch_ln_bw_fused<float>(
+                (float *)dx, dgamma, dbeta, (const float *)dy, (const float *)x,
+                (const float *)gamma, mean, rstd, rows, hidden, part, vec, st));
+        case LS_F16:
+            return from_cuda(lsr::launch_ln_bw_fused<__half>(
+                (__half *)dx, dgamma, dbeta, (const __half *)dy, (const __half *)x,
+                (const __half *)gamma, mean, rstd, rows, hidden, part, vec, st));
+        case LS_BF16:
+            return from_cuda(lsr::launch_ln_bw_fused<__nv_bfloat16>(
+                (__nv_bfloat16 *)dx, dgamma, dbeta, (const __nv_bfloat16 *)dy,
+                (const __nv_bfloat16 *)x, (const __nv_bfloat16 *)gamma, mean, rstd, rows, hidden,
                 part, vec, st));
     }
     return LS_ERR_UNSUPPORTED;

@@ -323,6 +323,50 @@ cudaError_t launch_ln_dgdb(float *dgamma, float *dbeta, const T *dy, const T *x,
                       (const float *)part, nchunks, N);
 }
 
+// Fused LayerNorm backward: a fixed cut of the rows into ln_bw_fused_chunks
+// chunks (at most 456), one block per chunk.  At most two 16-byte chunks per
+// thread: the per-column accumulators then fit in registers next to the row
+// (one chunk per thread measured slower: more threads and barriers per row).
+#define LSR_FUSED_BW_BUCKETS(X)                                                 \
+    X(1, 1) X(1, 2) X(2, 2) X(4, 2) X(8, 2) X(16, 2) X(32, 2) X(64, 2) X(128, 2) \
+    X(256, 2) X(512, 2)
+constexpr int kFusedMaxCpt = 2;
+
+
+template <typename T>
+cudaError_t launch_ln_bw_fused(T *dx, float *dgamma, float *dbeta, const T *dy, const T *x,
+                               const T *gamma, const float *mean, const float *rstd,
+                               int64_t rows, int64_t N, float *part, bool vec, cudaStream_t st) {
+    constexpr int V = Traits<T>::kVec;
+    int tpr = 0, cpt = 0;
+    if (rows > 0 && vec && pick_bucket_dense(N / V, kFusedMaxCpt, kLnMaxTpr, &tpr, &cpt)) {
+        int64_t nparts = 0;
+        cudaError_t e = cudaErrorInvalidValue;
+#define X(TPR_, CPT_)                                                                       \
+    if (tpr == TPR_ && cpt == CPT_) {                                                       \
+        const int64_t rpc = ceil_div(rows, (int64_t)ln_bw_fused_chunks<TPR_, CPT_>());      \
+        nparts = ceil_div(rows, rpc);                                                       \
+        constexpr size_t smem = ln_bw_fused_smem<TPR_, CPT_, kLnDinpStages, V>();            \
+        ensure_dynamic_smem<ln_bw_fused_vec<T, TPR_, CPT_, kLnDinpStages>>(smem);            \
+        e = launch_pdl(ln_bw_fused_vec<T, TPR_, CPT_, kLnDinpStages>,                        \
+                       dim3((unsigned)nparts),                                               \
+                       dim3(ln_bw_fused_block<TPR_>()), smem, st, dx, part, dy, x, gamma,    \
+                       mean, rstd, rows, (int)N, rpc);                                       \
+    }
+        LSR_FUSED_BW_BUCKETS(X)
+#undef X
+        if (e != cudaSuccess) return e;
+        return launch_pdl(ln_dgdb_final, dim3((unsigned)ceil_div(N, kFinalCols)),
+                          dim3(kFinalCols * kFinalLanes), 0, st, dgamma, dbeta,
+                          (const float *)part, nparts, N);
+    }
+    // rows that take the scalar path, or wider than 2 * 512 vectors: the two
+    // kernels one after the other
+    cudaError_t e = launch_ln_dinp<T>(dx, dy, x, gamma, mean, rstd, rows, N, vec, st);
+    if (e != cudaSuccess) return e;
+    return launch_ln_dgdb<T>(dgamma, dbeta, dy, x, mean, rstd, rows, N, part, vec, st);
+}
+
 // RMSNorm gamma gradient: the LayerNorm column sums with mean 0 and no dbeta.
 template <typename T>
 cudaError_t launch_rms_dgamma(float *dgamma, const T *dy, const T *x, const float *rstd,
@@ -348,6 +392,9 @@ cudaError_t launch_rms_dgamma(float *dgamma, const T *dy, const T *x, const floa
     template cudaError_t launch_ln_dgdb<T>(float *, float *, const T *, const T *,             \
                                            const float *, const float *, int64_t, int64_t,     \
                                            float *, bool, cudaStream_t);                       \
+    template cudaError_t launch_ln_bw_fused<T>(T *, float *, float *, const T *, const T *,     \
+                                               const T *, const float *, const float *,         \
+                                               int64_t, int64_t, float *, bool, cudaStream_t);  \
     template cudaError_t launch_rms_fw<T>(T *, float *, const T *, const T *, int64_t, int64_t, \
                                           float, bool, cudaStream_t);                          \
     template cudaError_t launch_rms_dinp<T>(T *, const T *, const T *, const T *,              \

@@ -45,6 +45,16 @@ cudaError_t launch_ln_dgdb(float *dgamma, float *dbeta, const T *dy, const T *x,
                            const float *mean, const float *rstd, int64_t rows,
                            int64_t N, float *part, bool vec, cudaStream_t st);
 
+// Partial-sum slots the fused LayerNorm backward may use for `rows` rows:
+// one per row chunk, at most 456.
+int64_t ln_bw_fused_max_parts(int64_t rows);
+
+// Fused LayerNorm backward: dx, dgamma, dbeta from one read of dy and x.
+template <typename T>
+cudaError_t launch_ln_bw_fused(T *dx, float *dgamma, float *dbeta, const T *dy, const T *x,
+                               const T *gamma, const float *mean, const float *rstd,
+                               int64_t rows, int64_t N, float *part, bool vec, cudaStream_t st);
+
 // RMSNorm (no mean, no beta): forward, input gradient, gamma gradient.
 template <typename T>
 cudaError_t launch_rms_fw(T *y, float *rstd, const T *x, const T *gamma, int64_t rows, int64_t N,

@@ -300,6 +300,196 @@ ln_dinp_vec(T *dx, const T *dy, const T *x, const T *gamma, const float *mean,
 }
 
 // ----------------------------------------------------------------------------
+// Fused backward: dx, and the dgamma / dbeta partial sums of one row chunk,
+// from one read of dy and x.  Block b owns rows [b*rpc, (b+1)*rpc) (a fixed
+// cut of the rows, independent of the GPU); its G row groups split them into
+// contiguous runs and go through the same staged pipeline as ln_dinp_vec.
+// Each thread also accumulates dgamma += dy * xhat and dbeta += dy for its
+// columns; the G groups' sums are added in group order through shared memory
+// and written as the chunk's partial part[(b*2 + {0,1}) * N + col], which
+// ln_dgdb_final then sums over chunks in a fixed order.  The epilogue re-reads
+// the staged row instead of keeping g and xhat in registers (the stage is not
+// refilled before the next iteration).
+// ----------------------------------------------------------------------------
+// Threads of a fused-backward block: at least 256 (several row groups when a
+// group is smaller), so that the fixed grid of row chunks still fills an SM.
+template <int TPR>
+constexpr int ln_bw_fused_block() { return TPR < 256 ? 256 : TPR; }
+
+// Resident blocks per SM the fused backward is compiled for (its register
+// budget): one 512-thread block, else three 256-thread blocks when a thread
+// holds one 16-byte chunk of the row, two when it holds two.
+template <int TPR, int CPT>
+constexpr int ln_bw_fused_resident() {
+    return ln_bw_fused_block<TPR>() > 256 ? 1 : (CPT == 1 ? 3 : 2);
+}
+
+// Row chunks (= blocks) of the fused backward: the resident blocks of a
+// 152-SM GB300.  A constant of the bucket, not the device's SM count, so that
+// the summation order depends only on the problem.
+constexpr int kFusedMaxChunks = 3 * 152;
+template <int TPR, int CPT>
+constexpr int ln_bw_fused_chunks() { return 152 * ln_bw_fused_resident<TPR, CPT>(); }
+
+template <int TPR, int CPT, int S, int V>
+constexpr size_t ln_bw_fused_smem() {
+    // the stage ring, reused at the end for the [G][2][TPR*CPT*V] group sums
+    constexpr int BLOCK = ln_bw_fused_block<TPR>();
+    constexpr size_t ring = (size_t)S * BLOCK * (2 * CPT * 16 + 2 * 4);
+    constexpr size_t sums = (size_t)BLOCK * 2 * CPT * V * 4;
+    return ring > sums ? ring : sums;
+}
+
+// Block b owns rows [b*rpc, min(rows, (b+1)*rpc)) (blocks past the last row
+// own none and contribute zeros); its G row groups split them into
+// contiguous runs.  Per row: the input gradient as ln_dinp_vec computes it
+// (same staging, same fused two-sum reduction), and each thread adds dy*xhat
+// and dy into per-column accumulators.  At the end the groups' accumulators
+// are added in group order in shared memory and the block writes its chunk's
+// part[(b*2 + {0,1}) * N + col].  (Pairing blocks in a thread-block cluster
+// to add two chunks through distributed shared memory first measured no
+// faster: the cluster barrier waits for the block's last dx stores.)
+template <typename T, int TPR, int CPT, int S>
+__global__ void __launch_bounds__(ln_bw_fused_block<TPR>(), (ln_bw_fused_resident<TPR, CPT>()))
+ln_bw_fused_vec(T *dx, float *part, const T *dy, const T *x, const T *gamma, const float *mean,
+                const float *rstd, int64_t rows, int N, int64_t rows_per_chunk) {
+    pdl_begin();
+    using Tr = Traits<T>;
+    constexpr int V = Tr::kVec;
+    constexpr int H2 = V / 2;
+    constexpr int BLOCK = ln_bw_fused_block<TPR>();
+    constexpr int G = BLOCK / TPR;
+    constexpr int W = TPR * CPT * V;  // columns a row group covers (>= N)
+    extern __shared__ uint4 dsmem[];
+    uint4 *stage = dsmem;                                                    // [S][2][CPT][BLOCK]
+    float *stat = reinterpret_cast<float *>(dsmem + S * 2 * CPT * BLOCK);    // [S][2][BLOCK]
+    __shared__ float red[TPR > 32 ? 64 : 1];  // >= 2 * BLOCK / 32 and group_sum2's 48
+
+    const int tid = threadIdx.x;
+    const int lane = tid % TPR;
+    const int grp = tid / TPR;
+    const int nchunk = N / V;
+    const float invN = 1.f / (float)N;
+    const int64_t c0 = (int64_t)blockIdx.x * rows_per_chunk;
+    const int64_t c1 = c0 + rows_per_chunk < rows ? c0 + rows_per_chunk : rows;
+    const int64_t per = (rows_per_chunk + G - 1) / G;  // rows per group (uniform)
+    const int64_t rbeg = c0 + grp * per;
+    const int64_t rend = rbeg + per < c1 ? rbeg + per : c1;
+
+    uint4 gr[CPT];
+    float2 ag[CPT][H2], ab[CPT][H2];
+#pragma unroll
+    for (int k = 0; k < CPT; ++k) {
+        const int c = k * TPR + lane;
+        if (c < nchunk) gr[k] = ld_cached16(gamma + c * V);
+#pragma unroll
+        for (int h = 0; h < H2; ++h) ag[k][h] = ab[k][h] = f2(0.f);
+    }
+    int64_t inext = rbeg;
+    auto issue = [&](int s) {
+        if (inext < rend) {
+            const int64_t off = inext * (int64_t)N;
+#pragma unroll
+            for (int k = 0; k < CPT; ++k) {
+                const int c = k * TPR + lane;
+                if (c < nchunk) {
+                    cp_async16(&stage[((s * 2 + 0) * CPT + k) * BLOCK + tid], dy + off + c * V);
+                    cp_async16(&stage[((s * 2 + 1) * CPT + k) * BLOCK + tid], x + off + c * V);
+                }
+            }
+            cp_async4(&stat[(s * 2 + 0) * BLOCK + tid], mean + inext);
+            cp_async4(&stat[(s * 2 + 1) * BLOCK + tid], rstd + inext);
+        }
+        ++inext;
+        cp_async_commit();
+    };
+#pragma unroll
+    for (int s = 0; s < S - 1; ++s) issue(s);
+
+    int s_cur = 0, s_iss = S - 1;
+    for (int64_t k = 0; k < per; ++k) {
+        issue(s_iss);
+        s_iss = s_iss + 1 == S ? 0 : s_iss + 1;
+        cp_async_wait<S - 1>();
+
+        const int64_t row = rbeg + k;
+        const bool valid = row < rend;
+        const float mu = valid ? stat[(s_cur * 2 + 0) * BLOCK + tid] : 0.f;
+        const float rs = valid ? stat[(s_cur * 2 + 1) * BLOCK + tid] : 0.f;
+        float2 g[CPT][H2], xh[CPT][H2];
+        float2 s1 = f2(0.f), s2 = f2(0.f);
+#pragma unroll
+        for (int kk = 0; kk < CPT; ++kk) {
+            const int c = kk * TPR + lane;
+            if (valid && c < nchunk) {
+                float2 gv[H2];
+                unpack2<T>(stage[((s_cur * 2 + 0) * CPT + kk) * BLOCK + tid], g[kk]);
+                unpack2<T>(stage[((s_cur * 2 + 1) * CPT + kk) * BLOCK + tid], xh[kk]);
+                unpack2<T>(gr[kk], gv);
+#pragma unroll
+                for (int h = 0; h < H2; ++h) {
+                    // g[kk][h] still holds dy here: the column sums take it first
+                    ab[kk][h] = add2(ab[kk][h], g[kk][h]);
+                    xh[kk][h] = mul2(add2(xh[kk][h], f2(-mu)), f2(rs));
+                    ag[kk][h] = fma2(g[kk][h], xh[kk][h], ag[kk][h]);
+                    g[kk][h] = mul2(g[kk][h], gv[h]);
+                    s1 = add2(s1, g[kk][h]);
+                    s2 = fma2(g[kk][h], xh[kk][h], s2);
+                }
+            }
+        }
+        float a1 = s1.x + s1.y, a2 = s2.x + s2.y;
+        group_sum2_of<TPR, BLOCK>(a1, a2, red, grp);
+        const float2 na = f2(-a1 * invN), nb = f2(-a2 * invN);
+        const int64_t off = row * (int64_t)N;
+#pragma unroll
+        for (int kk = 0; kk < CPT; ++kk) {
+            const int c = kk * TPR + lane;
+            if (valid && c < nchunk) {
+                float2 ov[H2];
+#pragma unroll
+                for (int h = 0; h < H2; ++h)
+                    ov[h] = mul2(f2(rs), fma2(xh[kk][h], nb, add2(g[kk][h], na)));
+                st_stream16(dx + off + c * V, pack2<T>(ov));
+            }
+        }
+        s_cur = s_cur + 1 == S ? 0 : s_cur + 1;
+    }
+
+    // block sums: the groups' accumulators in group order, into gs[0][.][.]
+    __syncthreads();  // every group is past its last read of the ring
+    float *gs = reinterpret_cast<float *>(dsmem);  // [G][2][W]
+#pragma unroll
+    for (int kk = 0; kk < CPT; ++kk) {
+        const int c = kk * TPR + lane;
+#pragma unroll
+        for (int h = 0; h < H2; ++h) {
+            gs[(grp * 2 + 0) * W + c * V + 2 * h] = ag[kk][h].x;
+            gs[(grp * 2 + 0) * W + c * V + 2 * h + 1] = ag[kk][h].y;
+            gs[(grp * 2 + 1) * W + c * V + 2 * h] = ab[kk][h].x;
+            gs[(grp * 2 + 1) * W + c * V + 2 * h + 1] = ab[kk][h].y;
+        }
+    }
+    __syncthreads();
+    if constexpr (G > 1) {
+        for (int col = tid; col < N; col += BLOCK) {
+            float a = gs[col], b = gs[W + col];
+            for (int gg = 1; gg < G; ++gg) {
+                a += gs[(gg * 2 + 0) * W + col];
+                b += gs[(gg * 2 + 1) * W + col];
+            }
+            gs[col] = a;  // each column is read and written by this thread only
+            gs[W + col] = b;
+        }
+    }
+    __syncthreads();
+    for (int col = tid; col < N; col += BLOCK) {
+        part[((int64_t)blockIdx.x * 2 + 0) * N + col] = gs[col];
+        part[((int64_t)blockIdx.x * 2 + 1) * N + col] = gs[W + col];
+    }
+}
+
+// ----------------------------------------------------------------------------
 // Looped variants (scalar accesses, any alignment, any row length).
 // ----------------------------------------------------------------------------
 template <typename T, int TPR, bool RMS>

@@ -298,6 +298,42 @@ __device__ __forceinline__ void group_sum2(float &a, float &b, float *smem) {
     }
 }
 
+// group_sum2 for blocks of several row groups (BLOCK / TPR of them) with
+// TPR > 32: each group's warps write their own slots and read back only those,
+// in warp order, so a row's sums are bitwise those of a one-group block.
+// `smem` holds 2 * BLOCK / 32 floats.  The group synchronises on its own
+// named barrier (1 + grp, TPR threads), so groups do not wait on one another.
+template <int TPR, int BLOCK>
+__device__ __forceinline__ void group_sum2_of(float &a, float &b, float *smem, int grp) {
+    if constexpr (TPR <= 32 || BLOCK == TPR) {
+        group_sum2<TPR>(a, b, smem);
+    } else {
+        constexpr int NW = TPR / 32;
+        constexpr int BW = BLOCK / 32;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            a += __shfl_xor_sync(0xffffffffu, a, o);
+            b += __shfl_xor_sync(0xffffffffu, b, o);
+        }
+        static_assert(BLOCK / TPR <= 15, "named barriers 1..15");
+        const int warp = threadIdx.x >> 5;
+        if ((threadIdx.x & 31) == 0) {
+            smem[warp] = a;
+            smem[BW + warp] = b;
+        }
+        asm volatile("bar.sync %0, %1;" ::"r"(1 + grp), "r"(TPR) : "memory");
+        const int w0 = grp * NW;
+        a = smem[w0];
+        b = smem[BW + w0];
+#pragma unroll
+        for (int w = 1; w < NW; ++w) {
+            a += smem[w0 + w];
+            b += smem[BW + w0 + w];
+        }
+        asm volatile("bar.sync %0, %1;" ::"r"(1 + grp), "r"(TPR) : "memory");
+    }
+}
+
 // Online (max, sum-of-exp2) pair, merged across a row group; used by the
 // looped path for rows longer than the register-resident buckets.  The pair
 // (m, s) stands for s * 2^m; m = -inf means "no finite element yet".

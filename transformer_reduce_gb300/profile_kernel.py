@@ -3,8 +3,8 @@
     python -m transformer_reduce_gb300.profile_kernel KERNEL [--workload W] [--launches N]
     python -m transformer_reduce_gb300.profile_kernel --sweep [--launches N]
 
-KERNEL is softmax_fw, softmax_bw, softmax_bw_masked, ln_fw, ln_dinp, ln_dgdb, rms_fw
-or rms_dinp.  Only the
+KERNEL is softmax_fw, softmax_bw, softmax_bw_masked, ln_fw, ln_dinp, ln_dgdb, ln_bw
+(the fused backward), rms_fw or rms_dinp.  Only the
 buffers that kernel touches are allocated (for the encoder workload at most
 ~0.8 GB), so a multi-pass ncu capture, which saves and restores device memory
 between passes, stays small while the tensors still exceed L2.
@@ -101,6 +101,18 @@ def prepare(kernel: str, case, dev):
             dx.data_ptr(), li["dy"].data_ptr(), li["x"].data_ptr(), li["gamma"].data_ptr(),
             mean.data_ptr(), rstd.data_ptr(), c.rows, c.hidden, _DT[c.dtype], st)), \
             traffic.layernorm_dinp_bytes(c.rows, c.hidden, c.dtype), keep
+    if kernel == "ln_bw":
+        n = _lib.ls_layernorm_bw_workspace_size(c.rows, c.hidden)
+        ws = torch.empty(max(n, 16) // 4, **f32)
+        dx = torch.empty_like(li["x"])
+        dg = torch.empty(c.hidden, **f32)
+        db = torch.empty(c.hidden, **f32)
+        keep = (li, ws, dx, dg, db, mean, rstd)
+        return (lambda: _lib.ls_layernorm_bw(
+            dx.data_ptr(), dg.data_ptr(), db.data_ptr(), li["dy"].data_ptr(), li["x"].data_ptr(),
+            li["gamma"].data_ptr(), mean.data_ptr(), rstd.data_ptr(), c.rows, c.hidden,
+            ws.data_ptr(), ws.numel() * 4, _DT[c.dtype], st)), \
+            traffic.layernorm_bw_fused_bytes(c.rows, c.hidden, c.dtype), keep
     n = _lib.ls_layernorm_bw_dgamma_dbeta_workspace_size(c.rows, c.hidden)
     ws = torch.empty(max(n, 16) // 4, **f32)
     dg = torch.empty(c.hidden, **f32)
@@ -134,11 +146,12 @@ def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("kernel", nargs="?",
                     choices=["softmax_fw", "softmax_bw", "softmax_bw_masked", "ln_fw", "ln_dinp",
-                             "ln_dgdb", "rms_fw", "rms_dinp"])
+                             "ln_dgdb", "ln_bw", "rms_fw", "rms_dinp"])
     ap.add_argument("--workload", default="encoder_big",
                     help="softmax or LayerNorm case name (encoder_big picks the encoder's case)")
     ap.add_argument("--launches", type=int, default=3)
     ap.add_argument("--sweep", action="store_true")
+    ap.add_argument("--only", default="", help="comma-separated kernels for --sweep")
     a = ap.parse_args(argv)
     build.build()
     dev = torch.device("cuda", 0)
@@ -152,8 +165,11 @@ def main(argv=None):
             pass
         jobs = [(k, c) for k in ("softmax_fw", "softmax_bw", "softmax_bw_masked")
                 for c in SOFTMAX_CASES.values()]
-        jobs += [(k, c) for k in ("ln_fw", "ln_dinp", "ln_dgdb", "rms_fw", "rms_dinp")
+        jobs += [(k, c) for k in ("ln_fw", "ln_dinp", "ln_dgdb", "ln_bw", "rms_fw", "rms_dinp")
                  for c in LN_CASES.values()]
+        if a.only:
+            keep_k = set(a.only.split(","))
+            jobs = [(k, c) for k, c in jobs if k in keep_k]
         for kernel, case in jobs:
             call, nbytes, keep = prepare(kernel, case, dev)
             ms = time_kernel(call, max(a.launches, 5), dev)

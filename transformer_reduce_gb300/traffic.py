@@ -10,6 +10,7 @@ Per row (Tk keys, N features):
   LN fw      : reads x (N), writes y (N) and mean, rstd (8 bytes)
   LN dinp    : reads dy, x (2N) and mean, rstd, writes dx (N)
   LN dg/db   : reads dy, x (2N) and mean, rstd
+  LN bw, fused : reads dy, x (2N) and mean, rstd, writes dx (N)
   RMS fw     : reads x (N), writes y (N) and rstd (4 bytes)
   RMS dinp   : reads dy, x (2N) and rstd, writes dx (N)
 plus the per-call operands read once (mask [B, Tk]; gamma, beta [N]) and
@@ -77,6 +78,13 @@ def layernorm_dinp_bytes(rows, N, dtype) -> int:
 def layernorm_dgdb_bytes(rows, N, dtype) -> int:
     s = ELEM_BYTES[dtype]
     return rows * (2 * N * s + 8) + 2 * N * 4
+
+
+def layernorm_bw_fused_bytes(rows, N, dtype) -> int:
+    """dx, dgamma and dbeta from one read of dy and x: the dinp bytes plus the
+    two fp32 gradient vectors."""
+    s = ELEM_BYTES[dtype]
+    return rows * (3 * N * s + 8) + N * s + 2 * N * 4
 
 
 def rmsnorm_fw_bytes(rows, N, dtype) -> int:
