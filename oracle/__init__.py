@@ -13,7 +13,8 @@ Sources are cited in ``ref_reduce.c``: the pages "CMU 11-868 L10:
 Accelerating Transformers on GPUs, and Where LightSeq Finds the Time"
 (section "Technique 2", slides 21-24) and "CMU 11-868 HW4：把 Softmax 與
 LayerNorm 寫成 CUDA 融合 kernel" (Problems 1.1-2.2 and the test baseline
-softmax(inp + mask)).
+softmax(inp + mask)); the L10 page's "Technique 1" (slide 12) for the cross
+entropy reduce kernel, and the FastTransformer page's section 5.4 for RMSNorm.
 
 Every function here is pinned by ``tests/test_oracle_pins.py`` to facts that
 do not come from the oracle itself (closed forms, invariants, finite
@@ -87,6 +88,11 @@ def _load():
         lib.ref_rmsnorm_bw_dinp.argtypes = [dp, dp, dp, dp, dp, i64, i64]
         lib.ref_rmsnorm_bw_dinp.restype = None
         lib.ref_rmsnorm_bw_dgamma.argtypes = [dp, dp, dp, dp, i64, i64]
+        i32p = ctypes.POINTER(ctypes.c_int32)
+        lib.ref_cross_entropy_fw.argtypes = [dp, dp, dp, i32p, i64, i64]
+        lib.ref_cross_entropy_fw.restype = None
+        lib.ref_cross_entropy_bw.argtypes = [dp, dp, i32p, dp, dp, i64, i64]
+        lib.ref_cross_entropy_bw.restype = None
         lib.ref_rmsnorm_bw_dgamma.restype = None
         _lib = lib
         return lib
@@ -293,3 +299,34 @@ def rmsnorm_bw_dgamma(dy, x, rstd):
     dg = np.empty(n)
     _load().ref_rmsnorm_bw_dgamma(_ptr(dg), _ptr(dy), _ptr(x), _ptr(rstd), rows, n)
     return dg
+
+
+def _i32(a) -> np.ndarray:
+    if hasattr(a, "detach"):
+        a = a.detach().cpu().numpy()
+    return np.ascontiguousarray(np.asarray(a, dtype=np.int32))
+
+
+def cross_entropy_fw(z, target):
+    """Softmax cross entropy of each row of z [rows, V] against its int32
+    target class; returns (loss, lse) float64 [rows].  target < 0: ignored
+    row (0, 0); target >= V: NaN."""
+    z, target = _f64(z), _i32(target)
+    rows, v = z.shape
+    assert target.shape == (rows,)
+    loss = np.empty(rows)
+    lse = np.empty(rows)
+    _load().ref_cross_entropy_fw(_ptr(loss), _ptr(lse), _ptr(z), _ptr(target, ctypes.c_int32),
+                                 rows, v)
+    return loss, lse
+
+
+def cross_entropy_bw(z, target, lse, dloss):
+    """dz = dloss * (softmax(z) - onehot(target)) from the saved log-sum-exp."""
+    z, lse, dloss, target = _f64(z), _f64(lse), _f64(dloss), _i32(target)
+    rows, v = z.shape
+    assert target.shape == (rows,) and lse.shape == (rows,) and dloss.shape == (rows,)
+    dz = np.empty_like(z)
+    _load().ref_cross_entropy_bw(_ptr(dz), _ptr(z), _ptr(target, ctypes.c_int32), _ptr(lse),
+                                 _ptr(dloss), rows, v)
+    return dz

@@ -37,6 +37,17 @@
  *         Co-Design", section 5.4 "Vectorized Pre-RMSNorm": RMSNorm, the
  *         LayerNorm without mean centring (scale only, no bias).
  *
+ *   [L10-T1] the L10 page, section "Technique 1: kernel fusion, leaving only
+ *         GEMMs to cuBLAS" (slide 12): cross entropy is the third custom
+ *         reduce kernel of the layer, beside LayerNorm and softmax.  The page
+ *         gives no formula; the oracle takes the textbook softmax cross
+ *         entropy of one target class per row.  Readings: int32 targets; a
+ *         negative target marks an ignored (padding) row, whose loss, saved
+ *         log-sum-exp and gradient are 0; a target >= V gives NaN loss and
+ *         gradient; no label smoothing; one loss per row (the caller
+ *         reduces); the backward takes the saved log-sum-exp and a per-row
+ *         upstream gradient.
+ *
  * Functions take row-major double arrays; the Python wrapper in this package
  * converts the storage-dtype inputs exactly (every fp32/fp16/bf16 value is a
  * double) and rounds nothing on the way in.
@@ -414,5 +425,68 @@ void ref_rmsnorm_bw_dgamma(double *dgamma, const double *dy, const double *x,
         for (int64_t r = 0; r < rows; ++r)
             dg += dy[r * N + j] * (x[r * N + j] * rstd[r]);
         dgamma[j] = dg;
+    }
+}
+
+/* ------------------------------------------------------------------------ */
+/* Cross entropy over a vocabulary                            [L10-T1]      */
+/* ------------------------------------------------------------------------ */
+/*
+ * For each row r of logits z [rows, V] with target class t = target[r]:
+ *   m      = max_j z_j
+ *   lse_r  = m + log( sum_j exp(z_j - m) )     (log of the softmax denominator)
+ *   loss_r = lse_r - z_t                       (= -log softmax(z)_t)
+ * t < 0  : ignored row, loss_r = lse_r = 0 (the row is not read).
+ * t >= V : loss_r = lse_r = NaN.
+ */
+void ref_cross_entropy_fw(double *loss, double *lse, const double *z, const int32_t *target,
+                          int64_t rows, int64_t V)
+{
+    for (int64_t r = 0; r < rows; ++r) {
+        const int32_t t = target[r];
+        if (t < 0) {
+            loss[r] = 0.0;
+            lse[r] = 0.0;
+            continue;
+        }
+        if ((int64_t)t >= V) {
+            loss[r] = NAN;
+            lse[r] = NAN;
+            continue;
+        }
+        const double *zr = z + r * V;
+        double m = -INFINITY;
+        for (int64_t j = 0; j < V; ++j)
+            if (zr[j] > m) m = zr[j];
+        double s = 0.0;
+        for (int64_t j = 0; j < V; ++j)
+            s += exp(zr[j] - m);
+        lse[r] = m + log(s);
+        loss[r] = lse[r] - zr[t];
+    }
+}
+
+/*
+ * Gradient of loss_r with respect to the logits, scaled by the upstream
+ * gradient dloss_r of that row:
+ *   dz_j = dloss_r * ( exp(z_j - lse_r) - [j == t] )
+ * (softmax minus the one-hot target).  Ignored rows (t < 0) get 0; t >= V
+ * gets NaN.
+ */
+void ref_cross_entropy_bw(double *dz, const double *z, const int32_t *target,
+                          const double *lse, const double *dloss, int64_t rows, int64_t V)
+{
+    for (int64_t r = 0; r < rows; ++r) {
+        const int32_t t = target[r];
+        double *dzr = dz + r * V;
+        const double *zr = z + r * V;
+        for (int64_t j = 0; j < V; ++j) {
+            if (t < 0)
+                dzr[j] = 0.0;
+            else if ((int64_t)t >= V)
+                dzr[j] = NAN;
+            else
+                dzr[j] = dloss[r] * (exp(zr[j] - lse[r]) - (j == t ? 1.0 : 0.0));
+        }
     }
 }

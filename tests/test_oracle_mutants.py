@@ -51,6 +51,18 @@ MUTANTS = [
     ("rms_bw_drop_term", "dxr[j] = rstd[r] * (g - xhat * b);", "dxr[j] = rstd[r] * g;", 0),
     ("rms_bw_sign", "dxr[j] = rstd[r] * (g - xhat * b);", "dxr[j] = rstd[r] * (g + xhat * b);", 0),
     ("rms_dgamma_no_rstd", "dg += dy[r * N + j] * (x[r * N + j] * rstd[r]);", "dg += dy[r * N + j] * x[r * N + j];", 0),
+    ("ce_no_max_shift", "s += exp(zr[j] - m);", "s += exp(zr[j]);", 0),
+    ("ce_lse_drops_max", "lse[r] = m + log(s);", "lse[r] = log(s);", 0),
+    ("ce_loss_sign", "loss[r] = lse[r] - zr[t];", "loss[r] = lse[r] + zr[t];", 0),
+    ("ce_loss_wrong_class", "loss[r] = lse[r] - zr[t];", "loss[r] = lse[r] - zr[0];", 0),
+    ("ce_bw_ignored_row_kept", "if (t < 0)\n                dzr[j] = 0.0;",
+     "if (t < -1000)\n                dzr[j] = 0.0;", 0),
+    ("ce_bw_onehot_sign", "(exp(zr[j] - lse[r]) - (j == t ? 1.0 : 0.0))",
+     "(exp(zr[j] - lse[r]) + (j == t ? 1.0 : 0.0))", 0),
+    ("ce_bw_onehot_off_by_one", "(j == t ? 1.0 : 0.0)", "(j == t + 1 ? 1.0 : 0.0)", 0),
+    ("ce_bw_no_dloss", "dzr[j] = dloss[r] * (exp(zr[j] - lse[r])", "dzr[j] = 1.0 * (exp(zr[j] - lse[r])", 0),
+    ("ce_bw_out_of_range_kept", "else if ((int64_t)t >= V)\n                dzr[j] = NAN;",
+     "else if ((int64_t)t >= V + 1)\n                dzr[j] = NAN;", 0),
     ("masked_bw_sum_all_keys", "if (visible(mr, k, q, offset, causal))\n                s += yr[k] * dyr[k];",
      "s += yr[k] * dyr[k];", 0),
     ("masked_bw_no_zeroing", "dxr[j] = visible(mr, j, q, offset, causal) ? yr[j] * (dyr[j] - s) : 0.0;",

@@ -484,3 +484,104 @@ def test_rmsnorm_bw_matches_torch_autograd(ref):
                                x.grad.numpy(), rtol=1e-11, atol=1e-12)
     np.testing.assert_allclose(ref.rmsnorm_bw_dgamma(dy.numpy(), x.detach().numpy(), rstd),
                                g.grad.numpy(), rtol=1e-11, atol=1e-12)
+
+
+# ----------------------------------------------------------------------------
+# cross entropy over a vocabulary (L10 page, "Technique 1", slide 12: the
+# third reduce kernel; the textbook softmax cross entropy)
+# ----------------------------------------------------------------------------
+
+def test_cross_entropy_fw_closed_forms(ref):
+    # equal logits: every class has probability 1/V, loss = log V
+    z = np.full((3, 7), 0.375)
+    loss, lse = ref.cross_entropy_fw(z, np.array([0, 3, 6]))
+    np.testing.assert_allclose(loss, math.log(7), rtol=1e-15)
+    np.testing.assert_allclose(lse, 0.375 + math.log(7), rtol=1e-15)
+    # two classes: loss = log(1 + exp(other - target)), the softplus
+    a, b = 1.25, -0.5
+    loss, _ = ref.cross_entropy_fw(np.array([[a, b], [a, b]]), np.array([0, 1]))
+    assert loss[0] == pytest.approx(math.log1p(math.exp(b - a)), rel=1e-14)
+    assert loss[1] == pytest.approx(math.log1p(math.exp(a - b)), rel=1e-14)
+
+
+def test_cross_entropy_fw_matches_scipy_and_torch(ref):
+    rng = np.random.default_rng(81)
+    rows, v = 19, 301
+    z = rng.normal(0, 3, size=(rows, v))
+    t = rng.integers(0, v, size=rows)
+    loss, lse = ref.cross_entropy_fw(z, t)
+    np.testing.assert_allclose(lse, scipy.special.logsumexp(z, axis=1), rtol=1e-14)
+    want = torch.nn.functional.cross_entropy(torch.tensor(z), torch.tensor(t), reduction="none")
+    np.testing.assert_allclose(loss, want.numpy(), rtol=1e-12, atol=1e-13)
+    # exp(-loss) is the softmax probability of the target class
+    p = ref.softmax_fw(z)
+    np.testing.assert_allclose(np.exp(-loss), p[np.arange(rows), t], rtol=1e-12)
+
+
+def test_cross_entropy_fw_large_logits_and_shift(ref):
+    rng = np.random.default_rng(82)
+    z = rng.normal(0, 1, size=(4, 50))
+    t = np.array([0, 7, 49, 21])
+    loss, lse = ref.cross_entropy_fw(z, t)
+    loss2, lse2 = ref.cross_entropy_fw(z + 1.0e4, t)  # exp would overflow without the max shift
+    assert np.all(np.isfinite(loss2))
+    np.testing.assert_allclose(loss2, loss, atol=1e-9)
+    np.testing.assert_allclose(lse2 - 1.0e4, lse, atol=1e-9)
+
+
+def test_cross_entropy_ignored_and_out_of_range_targets(ref):
+    rng = np.random.default_rng(83)
+    z = rng.normal(0, 2, size=(4, 9))
+    t = np.array([-1, 3, 9, -100])
+    loss, lse = ref.cross_entropy_fw(z, t)
+    assert loss[0] == 0.0 and lse[0] == 0.0 and loss[3] == 0.0 and lse[3] == 0.0
+    assert math.isnan(loss[2]) and math.isnan(lse[2])
+    assert loss[1] == pytest.approx(scipy.special.logsumexp(z[1]) - z[1, 3], rel=1e-14)
+    dz = ref.cross_entropy_bw(z, t, lse, np.ones(4))
+    assert np.all(dz[0] == 0.0) and np.all(dz[3] == 0.0) and np.all(np.isnan(dz[2]))
+    # NaN for a target >= V even when the saved log-sum-exp is finite
+    assert np.all(np.isnan(ref.cross_entropy_bw(z, t, np.zeros(4), np.ones(4))[2]))
+    # an ignored row is not read: NaN logits there change nothing
+    z2 = z.copy()
+    z2[0] = np.nan
+    l2, s2 = ref.cross_entropy_fw(z2, t)
+    assert l2[0] == 0.0 and s2[0] == 0.0
+    assert np.all(ref.cross_entropy_bw(z2, t, s2, np.ones(4))[0] == 0.0)
+
+
+@pytest.mark.parametrize("rows,v", [(3, 5), (2, 11)])
+def test_cross_entropy_bw_central_differences(ref, rows, v):
+    rng = np.random.default_rng(84)
+    z = rng.normal(0, 2, size=(rows, v))
+    t = rng.integers(0, v, size=rows)
+    dloss = rng.uniform(0.5, 2.0, size=rows)
+
+    def total(zz):
+        return float(np.sum(dloss * ref.cross_entropy_fw(zz, t)[0]))
+
+    _, lse = ref.cross_entropy_fw(z, t)
+    dz = ref.cross_entropy_bw(z, t, lse, dloss)
+    h = 1e-6
+    fd = np.zeros_like(z)
+    for idx in np.ndindex(z.shape):
+        zp, zm = z.copy(), z.copy()
+        zp[idx] += h
+        zm[idx] -= h
+        fd[idx] = (total(zp) - total(zm)) / (2 * h)
+    assert np.max(np.abs(dz - fd)) <= 1e-7 * max(1.0, np.max(np.abs(fd)))
+    # rows of the gradient sum to zero; only the target entry is negative
+    np.testing.assert_allclose(dz.sum(axis=1), 0.0, atol=1e-14)
+    for r in range(rows):
+        assert dz[r, t[r]] < 0 and np.all(np.delete(dz[r], t[r]) > 0)
+
+
+def test_cross_entropy_bw_matches_torch_autograd(ref):
+    rng = np.random.default_rng(85)
+    rows, v = 7, 129
+    z = torch.tensor(rng.normal(0, 3, size=(rows, v)), requires_grad=True)
+    t = torch.tensor(rng.integers(0, v, size=rows))
+    dl = torch.tensor(rng.normal(size=rows))
+    torch.nn.functional.cross_entropy(z, t, reduction="none").backward(dl)
+    _, lse = ref.cross_entropy_fw(z.detach().numpy(), t.numpy())
+    np.testing.assert_allclose(ref.cross_entropy_bw(z.detach().numpy(), t.numpy(), lse, dl.numpy()),
+                               z.grad.numpy(), rtol=1e-11, atol=1e-13)
