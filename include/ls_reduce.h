@@ -333,6 +333,53 @@ ls_status ls_rmsnorm_bw_dgamma(float *dgamma, const void *dy, const void *x, con
                                int64_t rows, int64_t hidden, void *workspace,
                                size_t workspace_bytes, ls_dtype dt, void *stream);
 
+/*
+ * Softmax cross entropy over a vocabulary, forward.  The L10 page, section
+ * "Technique 1: kernel fusion, leaving only GEMMs to cuBLAS" (slide 12),
+ * makes cross entropy the third custom reduce kernel beside LayerNorm and
+ * softmax; the page gives no formula, so this is the textbook one, in FP32.
+ * For each row r of logits z [rows, vocab] with target class t = target[r]:
+ *     lse_r  = log sum_j exp(z_rj)        (computed as max + log sum exp(z - max))
+ *     loss_r = lse_r - z_rt               (= -log softmax(z_r)_t)
+ * A negative target marks an ignored row (padding): loss_r = lse_r = 0 and
+ * the row is not read.  A target >= vocab gives loss_r = lse_r = NaN (there
+ * is no device-side trap).  No label smoothing; one loss per row (the caller
+ * reduces, e.g. sums over its non-ignored rows).
+ *
+ *   loss, lse  [rows] float32, device, written.
+ *   logits     [rows, vocab] dt, device, read; any vocab >= 1 (rows need
+ *              not start on 16-byte boundaries).
+ *   target     [rows] int32, device, read.
+ * Errors: LS_ERR_INVALID_ARG for rows < 0, vocab < 1 or a NULL pointer when
+ * rows > 0; LS_ERR_UNSUPPORTED for an unknown dtype or vocab above
+ * LS_MAX_ROW_LENGTH; LS_ERR_MISALIGNED for a pointer not aligned to its
+ * element; LS_ERR_CUDA for a failed launch.  rows == 0 launches nothing.
+ */
+ls_status ls_cross_entropy_fw(float *loss, float *lse, const void *logits,
+                              const int32_t *target, int64_t rows, int64_t vocab,
+                              ls_dtype dt, void *stream);
+
+/*
+ * Softmax cross entropy, backward: the gradient of loss_r * dloss_r with
+ * respect to the logits, from the lse saved by the forward:
+ *     dlogits_rj = dloss_r * ( exp(z_rj - lse_r) - [j == t_r] )
+ * Ignored rows (t_r < 0) are written as zeros and rows with t_r >= vocab as
+ * NaN; neither is read.
+ *
+ *   dlogits  [rows, vocab] dt, device, written.  May equal logits.
+ *   logits   [rows, vocab] dt, device, read.
+ *   target   [rows] int32, device, read.
+ *   lse      [rows] float32, device, read (as written by ls_cross_entropy_fw).
+ *   dloss    [rows] float32, device, read (upstream gradient of each row's
+ *            loss; 1 / (number of non-ignored rows) for a mean loss).
+ * Errors as for ls_cross_entropy_fw.  When logits and dlogits do not sit at
+ * the same offset modulo 16 bytes, every element is moved singly (slower,
+ * same result).
+ */
+ls_status ls_cross_entropy_bw(void *dlogits, const void *logits, const int32_t *target,
+                              const float *lse, const float *dloss, int64_t rows,
+                              int64_t vocab, ls_dtype dt, void *stream);
+
 /* Static, human-readable name of a status code (never NULL). */
 const char *ls_status_string(ls_status s);
 

@@ -96,6 +96,18 @@ def test_rejections_before_launch(abi):
     assert abi.ls_rmsnorm_fw(None, None, None, None, 0, 8, 1e-6, F32) == abi.LS_OK
     assert abi.ls_rmsnorm_bw_dinp(fake, fake, fake, fake, fake + 2, 4, 8, F32) == abi.LS_ERR_MISALIGNED
     assert abi.ls_rmsnorm_bw_dgamma(fake, fake, fake, fake, 16384, 1024, None, 0, BF16) == abi.LS_ERR_WORKSPACE
+    # cross entropy
+    assert abi.ls_cross_entropy_fw(fake, fake, fake, fake, 4, 0, F32) == abi.LS_ERR_INVALID_ARG
+    assert abi.ls_cross_entropy_fw(fake, fake, fake, fake, -1, 9, F32) == abi.LS_ERR_INVALID_ARG
+    assert abi.ls_cross_entropy_fw(fake, None, fake, fake, 4, 9, F32) == abi.LS_ERR_INVALID_ARG
+    assert abi.ls_cross_entropy_fw(fake, fake, fake, fake + 2, 4, 9, F32) == abi.LS_ERR_MISALIGNED
+    assert abi.ls_cross_entropy_fw(fake, fake, fake + 1, fake, 4, 9, BF16) == abi.LS_ERR_MISALIGNED
+    assert abi.ls_cross_entropy_fw(fake, fake, fake, fake, 4, (1 << 30) + 1, F32) == abi.LS_ERR_UNSUPPORTED
+    assert abi.ls_cross_entropy_fw(fake, fake, fake, fake, 4, 9, 3) == abi.LS_ERR_UNSUPPORTED
+    assert abi.ls_cross_entropy_fw(None, None, None, None, 0, 9, F32) == abi.LS_OK
+    assert abi.ls_cross_entropy_bw(fake, fake, fake, fake, None, 4, 9, F32) == abi.LS_ERR_INVALID_ARG
+    assert abi.ls_cross_entropy_bw(fake, fake, fake, fake + 1, fake, 4, 9, F32) == abi.LS_ERR_MISALIGNED
+    assert abi.ls_cross_entropy_bw(None, None, None, None, None, 0, 9, BF16) == abi.LS_OK
     # fused LayerNorm backward
     nf = abi.ls_layernorm_bw_workspace_size(16384, 1024)
     assert abi.ls_layernorm_bw(fake, fake, fake, fake, fake, fake, fake, fake, 16384, 1024,

@@ -10,7 +10,7 @@ if the library is missing or a call fails, they raise.
 """
 from __future__ import annotations
 
-from ._lib import (LS_BF16, LS_ERR_CUDA, LS_ERR_INVALID_ARG, LS_ERR_MISALIGNED,  # noqa: F401
+from ._lib import (LS_BF16, LS_ERR_CUDA, ls_cross_entropy_bw, ls_cross_entropy_fw, LS_ERR_INVALID_ARG, LS_ERR_MISALIGNED,  # noqa: F401
                    LS_ERR_UNSUPPORTED, LS_ERR_WORKSPACE, LS_F16, LS_F32, LS_OK, LsError,
                    ls_layernorm_bw_dgamma_dbeta, ls_layernorm_bw_dgamma_dbeta_workspace_size,
                    ls_layernorm_bw, ls_layernorm_bw_dinp, ls_layernorm_bw_workspace_size,
@@ -21,7 +21,8 @@ from ._lib import (LS_BF16, LS_ERR_CUDA, LS_ERR_INVALID_ARG, LS_ERR_MISALIGNED, 
 __all__ = [
     "softmax_fw", "softmax_bw", "softmax_bw_masked", "layernorm_fw", "layernorm_bw_dinp",
     "layernorm_bw_dgamma_dbeta", "dgamma_dbeta_workspace", "layernorm_bw", "rmsnorm_fw", "rmsnorm_bw_dinp",
-    "rmsnorm_bw_dgamma", "LsError", "load",
+    "rmsnorm_bw_dgamma", "cross_entropy_fw", "cross_entropy_bw", "LsError", "load",
+    "ls_cross_entropy_fw", "ls_cross_entropy_bw",
     "ls_softmax_fw", "ls_softmax_bw", "ls_softmax_bw_masked", "ls_layernorm_fw", "ls_layernorm_bw_dinp",
     "ls_layernorm_bw_dgamma_dbeta", "ls_layernorm_bw_dgamma_dbeta_workspace_size",
     "ls_layernorm_bw", "ls_layernorm_bw_workspace_size", "ls_rmsnorm_fw", "ls_rmsnorm_bw_dinp", "ls_rmsnorm_bw_dgamma",
@@ -219,3 +220,32 @@ def rmsnorm_bw_dgamma(dy, x, rstd, workspace=None, dgamma=None):
                              _ptr(workspace), workspace.numel() * workspace.element_size(),
                              ls_dtype(x), _stream(x)), "ls_rmsnorm_bw_dgamma")
     return dgamma
+
+
+def cross_entropy_fw(logits, target, loss=None, lse=None):
+    """Per-row softmax cross entropy of logits [rows, vocab] against int32
+    target [rows] (negative = ignored row); returns (loss, lse), fp32."""
+    torch = _torch()
+    if logits.dim() != 2:
+        raise ValueError("logits must be [rows, vocab]")
+    rows, vocab = logits.shape
+    if tuple(target.shape) != (rows,) or target.dtype != torch.int32:
+        raise ValueError("target must be int32 [rows]")
+    loss = torch.empty(rows, device=logits.device, dtype=torch.float32) if loss is None else loss
+    lse = torch.empty(rows, device=logits.device, dtype=torch.float32) if lse is None else lse
+    _dev(logits, target, loss, lse)
+    _ok(ls_cross_entropy_fw(_ptr(loss), _ptr(lse), _ptr(logits), _ptr(target), rows, vocab,
+                            ls_dtype(logits), _stream(logits)), "ls_cross_entropy_fw")
+    return loss, lse
+
+
+def cross_entropy_bw(logits, target, lse, dloss, dlogits=None):
+    """Gradient dloss * (softmax(logits) - onehot(target)) per row, from the
+    forward's lse; ``dlogits`` may be ``logits`` (in place)."""
+    torch = _torch()
+    rows, vocab = logits.shape
+    dlogits = torch.empty_like(logits) if dlogits is None else dlogits
+    _dev(logits, target, lse, dloss, dlogits)
+    _ok(ls_cross_entropy_bw(_ptr(dlogits), _ptr(logits), _ptr(target), _ptr(lse), _ptr(dloss),
+                            rows, vocab, ls_dtype(logits), _stream(logits)), "ls_cross_entropy_bw")
+    return dlogits

@@ -40,6 +40,8 @@ SIGNATURES = {
     "ls_rmsnorm_fw": ([_VP, _VP, _VP, _VP, _I64, _I64, _F32, _INT, _VP], _INT),
     "ls_rmsnorm_bw_dinp": ([_VP, _VP, _VP, _VP, _VP, _I64, _I64, _INT, _VP], _INT),
     "ls_rmsnorm_bw_dgamma": ([_VP, _VP, _VP, _VP, _I64, _I64, _VP, _SZ, _INT, _VP], _INT),
+    "ls_cross_entropy_fw": ([_VP, _VP, _VP, _VP, _I64, _I64, _INT, _VP], _INT),
+    "ls_cross_entropy_bw": ([_VP, _VP, _VP, _VP, _VP, _I64, _I64, _INT, _VP], _INT),
     "ls_status_string": ([_INT], ctypes.c_char_p),
 }
 
@@ -138,3 +140,11 @@ def ls_rmsnorm_bw_dgamma(dgamma, dy, x, rstd, rows, hidden, workspace, workspace
                          stream=0) -> int:
     return load().ls_rmsnorm_bw_dgamma(dgamma, dy, x, rstd, rows, hidden, workspace,
                                        workspace_bytes, dt, stream)
+
+
+def ls_cross_entropy_fw(loss, lse, logits, target, rows, vocab, dt, stream=0) -> int:
+    return load().ls_cross_entropy_fw(loss, lse, logits, target, rows, vocab, dt, stream)
+
+
+def ls_cross_entropy_bw(dlogits, logits, target, lse, dloss, rows, vocab, dt, stream=0) -> int:
+    return load().ls_cross_entropy_bw(dlogits, logits, target, lse, dloss, rows, vocab, dt, stream)

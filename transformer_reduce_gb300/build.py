@@ -24,7 +24,8 @@ BUILD_DIR = os.path.join(ROOT, "_build")
 LIB_NAME = "libls_reduce.so"
 LIB_PATH = os.path.join(PKG, LIB_NAME)
 
-SOURCES = ["abi.cu", "kernels_f32.cu", "kernels_f16.cu", "kernels_bf16.cu", "noalloc.cu"]
+SOURCES = ["abi.cu", "kernels_f32.cu", "kernels_f16.cu", "kernels_bf16.cu", "noalloc.cu",
+           "cross_entropy.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-O2",
               "--expt-relaxed-constexpr"]

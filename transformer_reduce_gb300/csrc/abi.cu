@@ -448,4 +448,63 @@ ls_status ls_layernorm_bw_dgamma_dbeta(float *dgamma, float *dbeta, const void *
     return LS_ERR_UNSUPPORTED;
 }
 
+// ----------------------------------------------------------------------------
+// cross entropy over a vocabulary
+// ----------------------------------------------------------------------------
+ls_status ls_cross_entropy_fw(float *loss, float *lse, const void *logits, const int32_t *target,
+                              int64_t rows, int64_t vocab, ls_dtype dt, void *stream) {
+    const size_t es = elem_size(dt);
+    ls_status s = ln_check(rows, vocab, es);
+    if (s != LS_OK) return s;
+    if (rows > 0 && (!loss || !lse || !logits || !target)) return LS_ERR_INVALID_ARG;
+    if ((loss && !aligned(loss, 4)) || (lse && !aligned(lse, 4)) ||
+        (logits && !aligned(logits, es)) || (target && !aligned(target, 4)))
+        return LS_ERR_MISALIGNED;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    // the aligned middle of every row is read in 16-byte vectors whatever the
+    // row's start offset
+    switch (dt) {
+        case LS_F32:
+            return from_cuda(lsr::launch_ce_fw<float>(loss, lse, (const float *)logits, target,
+                                                      rows, vocab, true, st));
+        case LS_F16:
+            return from_cuda(lsr::launch_ce_fw<__half>(loss, lse, (const __half *)logits, target,
+                                                       rows, vocab, true, st));
+        case LS_BF16:
+            return from_cuda(lsr::launch_ce_fw<__nv_bfloat16>(
+                loss, lse, (const __nv_bfloat16 *)logits, target, rows, vocab, true, st));
+    }
+    return LS_ERR_UNSUPPORTED;
+}
+
+ls_status ls_cross_entropy_bw(void *dlogits, const void *logits, const int32_t *target,
+                              const float *lse, const float *dloss, int64_t rows, int64_t vocab,
+                              ls_dtype dt, void *stream) {
+    const size_t es = elem_size(dt);
+    ls_status s = ln_check(rows, vocab, es);
+    if (s != LS_OK) return s;
+    if (rows > 0 && (!dlogits || !logits || !target || !lse || !dloss)) return LS_ERR_INVALID_ARG;
+    if ((dlogits && !aligned(dlogits, es)) || (logits && !aligned(logits, es)) ||
+        (target && !aligned(target, 4)) || (lse && !aligned(lse, 4)) ||
+        (dloss && !aligned(dloss, 4)))
+        return LS_ERR_MISALIGNED;
+    // vectors need logits and dlogits at the same offset within 16 bytes
+    const bool vec =
+        ((reinterpret_cast<uintptr_t>(dlogits) ^ reinterpret_cast<uintptr_t>(logits)) & 15u) == 0;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    switch (dt) {
+        case LS_F32:
+            return from_cuda(lsr::launch_ce_bw<float>((float *)dlogits, (const float *)logits,
+                                                      target, lse, dloss, rows, vocab, vec, st));
+        case LS_F16:
+            return from_cuda(lsr::launch_ce_bw<__half>((__half *)dlogits, (const __half *)logits,
+                                                       target, lse, dloss, rows, vocab, vec, st));
+        case LS_BF16:
+            return from_cuda(lsr::launch_ce_bw<__nv_bfloat16>(
+                (__nv_bfloat16 *)dlogits, (const __nv_bfloat16 *)logits, target, lse, dloss, rows,
+                vocab, vec, st));
+    }
+    return LS_ERR_UNSUPPORTED;
+}
+
 }  // extern "C"

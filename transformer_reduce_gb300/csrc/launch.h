@@ -66,4 +66,15 @@ template <typename T>
 cudaError_t launch_rms_dgamma(float *dgamma, const T *dy, const T *x, const float *rstd,
                               int64_t rows, int64_t N, float *part, bool vec, cudaStream_t st);
 
+// Softmax cross entropy over a vocabulary (forward: loss and log-sum-exp per
+// row; backward: dz from the saved log-sum-exp).  vec: take 16-byte vectors
+// for the aligned middle of each row (the backward needs z and dz at the same
+// offset modulo 16 bytes).
+template <typename T>
+cudaError_t launch_ce_fw(float *loss, float *lse, const T *z, const int32_t *target, int64_t rows,
+                         int64_t V, bool vec, cudaStream_t st);
+template <typename T>
+cudaError_t launch_ce_bw(T *dz, const T *z, const int32_t *target, const float *lse,
+                         const float *dloss, int64_t rows, int64_t V, bool vec, cudaStream_t st);
+
 }  // namespace lsr

@@ -4,7 +4,8 @@
     python -m transformer_reduce_gb300.profile_kernel --sweep [--launches N]
 
 KERNEL is softmax_fw, softmax_bw, softmax_bw_masked, ln_fw, ln_dinp, ln_dgdb, ln_bw
-(the fused backward), rms_fw or rms_dinp.  Only the
+(the fused backward), rms_fw, rms_dinp, ce_fw or ce_bw (cross entropy; its
+workloads are the ce_* cases, ce_gpt2 by default).  Only the
 buffers that kernel touches are allocated (for the encoder workload at most
 ~0.8 GB), so a multi-pass ncu capture, which saves and restores device memory
 between passes, stays small while the tensors still exceed L2.
@@ -32,6 +33,7 @@ _DT = {"f32": _lib.LS_F32, "f16": _lib.LS_F16, "bf16": _lib.LS_BF16}
 SOFTMAX_CASES = {c.name: c for c in
                  [workloads.TINY["softmax"], workloads.GPT2_SMALL["softmax"],
                   *workloads.SOFTMAX_SWEEP, workloads.ENCODER_BIG["softmax"]]}
+CE_CASES = {c.name: c for c in workloads.CE_CASES}
 LN_CASES = {c.name: c for c in
             [workloads.TINY["layernorm"], workloads.GPT2_SMALL["layernorm"],
              *workloads.LAYERNORM_SWEEP, workloads.ENCODER_BIG["layernorm"][0]]}
@@ -45,6 +47,25 @@ def _ok(s, where):
 def prepare(kernel: str, case, dev):
     """(call, algorithmic bytes) for one kernel on one case; call() enqueues it."""
     st = torch.cuda.current_stream(dev).cuda_stream
+    if kernel.startswith("ce"):
+        ci = workloads.cross_entropy_inputs(case, device=dev)
+        z, t = ci["logits"], ci["target"]
+        valid = int((t >= 0).sum())
+        f32 = dict(device=dev, dtype=torch.float32)
+        loss = torch.empty(case.rows, **f32)
+        lse = torch.full((case.rows,), 12.0, **f32)
+        if kernel == "ce_fw":
+            keep = (z, t, loss, lse)
+            return (lambda: _lib.ls_cross_entropy_fw(
+                loss.data_ptr(), lse.data_ptr(), z.data_ptr(), t.data_ptr(), case.rows,
+                case.vocab, _DT[case.dtype], st)), \
+                traffic.cross_entropy_fw_bytes(case.rows, valid, case.vocab, case.dtype), keep
+        dz = torch.empty_like(z)
+        keep = (z, t, lse, dz, ci)
+        return (lambda: _lib.ls_cross_entropy_bw(
+            dz.data_ptr(), z.data_ptr(), t.data_ptr(), lse.data_ptr(), ci["dloss"].data_ptr(),
+            case.rows, case.vocab, _DT[case.dtype], st)), \
+            traffic.cross_entropy_bw_bytes(case.rows, valid, case.vocab, case.dtype), keep
     if kernel.startswith("softmax"):
         s = case
         inp = workloads.softmax_inputs(s, device=dev)
@@ -146,7 +167,7 @@ def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("kernel", nargs="?",
                     choices=["softmax_fw", "softmax_bw", "softmax_bw_masked", "ln_fw", "ln_dinp",
-                             "ln_dgdb", "ln_bw", "rms_fw", "rms_dinp"])
+                             "ln_dgdb", "ln_bw", "rms_fw", "rms_dinp", "ce_fw", "ce_bw"])
     ap.add_argument("--workload", default="encoder_big",
                     help="softmax or LayerNorm case name (encoder_big picks the encoder's case)")
     ap.add_argument("--launches", type=int, default=3)
@@ -167,6 +188,7 @@ def main(argv=None):
                 for c in SOFTMAX_CASES.values()]
         jobs += [(k, c) for k in ("ln_fw", "ln_dinp", "ln_dgdb", "ln_bw", "rms_fw", "rms_dinp")
                  for c in LN_CASES.values()]
+        jobs += [(k, c) for k in ("ce_fw", "ce_bw") for c in CE_CASES.values()]
         if a.only:
             keep_k = set(a.only.split(","))
             jobs = [(k, c) for k, c in jobs if k in keep_k]
@@ -185,7 +207,9 @@ def main(argv=None):
         return
     if a.kernel is None:
         ap.error("KERNEL or --sweep is required")
-    if a.workload == "encoder_big":
+    if a.kernel.startswith("ce"):
+        case = CE_CASES[a.workload if a.workload in CE_CASES else "ce_gpt2"]
+    elif a.workload == "encoder_big":
         case = workloads.ENCODER_BIG["softmax"] if a.kernel.startswith("softmax") \
             else workloads.ENCODER_BIG["layernorm"][0]
     else:

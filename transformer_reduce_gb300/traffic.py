@@ -13,6 +13,10 @@ Per row (Tk keys, N features):
   LN bw, fused : reads dy, x (2N) and mean, rstd, writes dx (N)
   RMS fw     : reads x (N), writes y (N) and rstd (4 bytes)
   RMS dinp   : reads dy, x (2N) and rstd, writes dx (N)
+  CE fw      : reads the V logits of each non-ignored row; per row the target
+               (4 bytes) and loss, lse (8 bytes)
+  CE bw      : reads the V logits of each non-ignored row; per row target, lse,
+               dloss (12 bytes) and dlogits (V) written for every row
 plus the per-call operands read once (mask [B, Tk]; gamma, beta [N]) and
 written once (dgamma, dbeta [N] fp32).  The FastTransformer page's figure of
 805 MB per step for writing and re-reading the (B,H,T,T) fp32 probability
@@ -95,3 +99,13 @@ def rmsnorm_fw_bytes(rows, N, dtype) -> int:
 def rmsnorm_dinp_bytes(rows, N, dtype) -> int:
     s = ELEM_BYTES[dtype]
     return rows * (3 * N * s + 4) + N * s
+
+
+def cross_entropy_fw_bytes(rows, valid_rows, V, dtype) -> int:
+    s = ELEM_BYTES[dtype]
+    return valid_rows * V * s + rows * 12
+
+
+def cross_entropy_bw_bytes(rows, valid_rows, V, dtype) -> int:
+    s = ELEM_BYTES[dtype]
+    return valid_rows * V * s + rows * (V * s + 12)

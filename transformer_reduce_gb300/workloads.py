@@ -167,3 +167,57 @@ def layernorm_inputs(case: LayerNormCase, device="cpu"):
         "beta": _normal((case.hidden,), 0.0, 0.1, dt, device, case.seed, "ln.beta"),
         "dy": _normal(shape, 0.0, 1.0, dt, device, case.seed, "ln.dy"),
     }
+
+
+# ----------------------------------------------------------------------------
+# cross entropy over a vocabulary
+# ----------------------------------------------------------------------------
+# One row per token: the GPT-2 decoder step above has B*T = 8,192 tokens.  The
+# pages give no vocabulary size; the stand-ins are GPT-2's byte-pair vocabulary
+# (50,257 entries: rows start off the 16-byte grid), the same padded to a
+# multiple of 64 (50,304), and a character vocabulary of 65 symbols for the
+# small case (the FastTransformer page trains on TinyShakespeare).
+@dataclasses.dataclass(frozen=True)
+class CrossEntropyCase:
+    name: str
+    B: int
+    T: int
+    vocab: int
+    pad: Optional[tuple]       # (lo, hi) valid tokens per sequence; the rest are ignored
+    logit_std: float
+    dtype: str
+    seed: int
+
+    @property
+    def rows(self):
+        return self.B * self.T
+
+
+CE_TINY = CrossEntropyCase("ce_tiny", 2, 32, 65, (16, 32), 3.0, "f32", 0)
+CE_GPT2 = CrossEntropyCase("ce_gpt2", 32, 256, 50257, None, 3.0, "f16", 1)
+CE_GPT2_PADDED = CrossEntropyCase("ce_gpt2_v50304", 32, 256, 50304, None, 3.0, "bf16", 1)
+CE_CASES = [CE_TINY, CE_GPT2, CE_GPT2_PADDED]
+
+
+def cross_entropy_inputs(case: CrossEntropyCase, device="cpu"):
+    """logits ~ N(0, std^2) [rows, vocab]; int32 targets uniform in [0, vocab),
+    -1 on the padded positions of each sequence; dloss = 1 / (valid rows)
+    on valid rows (a mean loss) and 0 elsewhere."""
+    dt = DTYPES[case.dtype]
+    logits = _normal((case.rows, case.vocab), 0.0, case.logit_std, dt, device, case.seed,
+                     "ce.logits")
+    g = torch.Generator().manual_seed(sub_seed(case.seed, "ce.target"))
+    target = torch.randint(0, case.vocab, (case.rows,), generator=g, dtype=torch.int64)
+    if case.pad is not None:
+        g2 = torch.Generator().manual_seed(sub_seed(case.seed, "ce.lengths"))
+        lens = torch.randint(case.pad[0], case.pad[1] + 1, (case.B,), generator=g2)
+        pos = torch.arange(case.T).view(1, case.T)
+        target = torch.where(pos < lens.view(case.B, 1), target.view(case.B, case.T),
+                             torch.full((), -1, dtype=torch.int64)).reshape(-1)
+    valid = target >= 0
+    dloss = valid.to(torch.float32) / max(1, int(valid.sum()))
+    return {
+        "logits": logits,
+        "target": target.to(torch.int32).to(device),
+        "dloss": dloss.to(device),
+    }
