@@ -25,13 +25,15 @@
 namespace lsr {
 
 // Threads per row: one warp for rows of up to 512 16-byte vectors, else one
-// 512-thread block.  A 256-thread block holds eight one-warp rows.
-constexpr int kCeWideTpr = 512;
+// 128-thread block (a GPT-2 vocabulary row is then ~100 vectors per thread,
+// and ~1,400 rows are in flight on 152 SMs: 8,192 rows make six even waves).
+// A 256-thread block holds eight one-warp rows.
+constexpr int kCeWideTpr = 128;
 constexpr int kCeNarrowMax = 512;  // vectors per row for the one-warp path
 constexpr int kCeUnroll = 4;       // 16-byte vectors in flight per thread
 
 template <int TPR>
-constexpr int ce_block() { return TPR < 256 ? 256 : TPR; }
+constexpr int ce_block() { return TPR < 128 ? 256 : TPR; }
 
 // Head / body / tail of a row that starts at p: `head` scalars up to the
 // first 16-byte boundary, then `nbody` whole vectors.  vec == false puts the
@@ -69,6 +71,30 @@ struct OnlineLse {
     }
 };
 
+// Sum of 2^(z*log2 e - m) over n logits into acc.  The running maximum is
+// only raised when a partial sum leaves the safe range (2^64: no overflow for
+// any chunk, and m never exceeds the true maximum, so no term that matters
+// underflows); most chunks therefore skip the per-logit max.  The first chunk
+// (m = -inf) always takes the slow path.  A NaN logit keeps the sum NaN.
+template <int N>
+__device__ __forceinline__ void ce_accumulate(OnlineLse &acc, const float (&f)[N]) {
+    float ps = 0.f;
+#pragma unroll
+    for (int e = 0; e < N; ++e) ps += fast_exp2(fmaf(f[e], kLog2e, -acc.m));
+    if (!(ps <= 0x1p64f)) {
+        float cm = -INFINITY;
+#pragma unroll
+        for (int e = 0; e < N; ++e) cm = fmaxf(cm, f[e]);
+        const float mn = acc.rebase(cm);
+        ps = 0.f;
+        if (mn != -INFINITY) {
+#pragma unroll
+            for (int e = 0; e < N; ++e) ps += fast_exp2(fmaf(f[e], kLog2e, -mn));
+        }
+    }
+    acc.s += ps;
+}
+
 template <typename T, int TPR>
 __global__ void __launch_bounds__(ce_block<TPR>())
 ce_fw_kernel(float *loss, float *lse, const T *z, const int32_t *target, int64_t rows, int64_t V,
@@ -78,6 +104,7 @@ ce_fw_kernel(float *loss, float *lse, const T *z, const int32_t *target, int64_t
     constexpr int VV = Tr::kVec;
     constexpr int BLOCK = ce_block<TPR>();
     constexpr int G = BLOCK / TPR;
+    constexpr int64_t STEP = (int64_t)kCeUnroll * TPR;
     __shared__ float red[64];
     const int lane = threadIdx.x % TPR;
     const int grp = threadIdx.x / TPR;
@@ -98,43 +125,38 @@ ce_fw_kernel(float *loss, float *lse, const T *z, const int32_t *target, int64_t
             for (int64_t j = head + nbody * VV + lane; j < V; j += TPR)
                 acc.add1(Tr::load1(zr + j));
             const T *zb = zr + head;
+            // groups of kCeUnroll vectors, the next group's loads issued
+            // before the current group is summed
             int64_t c = lane;
-            for (; c + (int64_t)(kCeUnroll - 1) * TPR < nbody; c += (int64_t)kCeUnroll * TPR) {
-                uint4 raw[kCeUnroll];
+            bool have = c + (int64_t)(kCeUnroll - 1) * TPR < nbody;
+            uint4 raw[kCeUnroll];
+            if (have) {
 #pragma unroll
                 for (int u = 0; u < kCeUnroll; ++u)
                     raw[u] = ld_stream16(zb + (c + (int64_t)u * TPR) * VV);
-                float f[kCeUnroll][VV];
-                float cm = -INFINITY;
+            }
+            while (have) {
+                float f[kCeUnroll * VV];
 #pragma unroll
                 for (int u = 0; u < kCeUnroll; ++u) {
-                    Tr::unpack(raw[u], f[u]);
+                    float g[VV];
+                    Tr::unpack(raw[u], g);
 #pragma unroll
-                    for (int e = 0; e < VV; ++e) cm = fmaxf(cm, f[u][e]);
+                    for (int e = 0; e < VV; ++e) f[u * VV + e] = g[e];
                 }
-                const float mn = acc.rebase(cm);
-                if (mn != -INFINITY) {
-                    float ps = 0.f;
+                c += STEP;
+                have = c + (int64_t)(kCeUnroll - 1) * TPR < nbody;
+                if (have) {
 #pragma unroll
                     for (int u = 0; u < kCeUnroll; ++u)
-#pragma unroll
-                        for (int e = 0; e < VV; ++e) ps += fast_exp2(fmaf(f[u][e], kLog2e, -mn));
-                    acc.s += ps;
+                        raw[u] = ld_stream16(zb + (c + (int64_t)u * TPR) * VV);
                 }
+                ce_accumulate(acc, f);
             }
             for (; c < nbody; c += TPR) {
                 float f[VV];
                 Tr::unpack(ld_stream16(zb + c * VV), f);
-                float cm = -INFINITY;
-#pragma unroll
-                for (int e = 0; e < VV; ++e) cm = fmaxf(cm, f[e]);
-                const float mn = acc.rebase(cm);
-                if (mn != -INFINITY) {
-                    float ps = 0.f;
-#pragma unroll
-                    for (int e = 0; e < VV; ++e) ps += fast_exp2(fmaf(f[e], kLog2e, -mn));
-                    acc.s += ps;
-                }
+                ce_accumulate(acc, f);
             }
         }
         group_ms_merge<TPR>(acc.m, acc.s, red);
