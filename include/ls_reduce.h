@@ -250,7 +250,10 @@ ls_status ls_layernorm_bw(void *dx, float *dgamma, float *dbeta, const void *dy,
 
 /*
  * Size of the device array that ls_layernorm_bw_dgamma_dbeta_noalloc uses as
- * scratch (4 MiB).  It covers, for example, [16384, 8192] and [16384, 1024].
+ * scratch (4 MiB).  It covers every problem with hidden <= 524288 (2^19),
+ * whatever the row count: the partial sums take at most 456 * 2048 bytes
+ * for hidden below 116736 (456 tiles of 256), and 8 * hidden bytes (one
+ * row chunk) above it.
  */
 #define LS_DGDB_NOALLOC_SCRATCH_BYTES ((size_t)4 << 20)
 

@@ -165,6 +165,16 @@ def test_fused_backward_workspace_size():
         assert n >= _lib.ls_layernorm_bw_dgamma_dbeta_workspace_size(rows, hidden)
 
 
+def test_no_alloc_scratch_covers_the_stated_widths(abi):
+    # the header's bound: every hidden <= 2^19 fits the 4 MiB array
+    ws = abi.ls_layernorm_bw_dgamma_dbeta_workspace_size
+    for hidden in [1, 255, 256, 257, 1000, 1024, 8192, 65536, 100003, 155647, 155648, 368640,
+                   524287, 1 << 19]:
+        for rows in [1, 15, 16, 17, 1000, 9727, 9728, 16384, 100000, 1 << 22]:
+            assert ws(rows, hidden) <= 4 << 20, (rows, hidden)
+    assert ws(1 << 16, (1 << 19) + 1) > 4 << 20
+
+
 def test_byte_model_reproduces_the_pages_figure():
     from transformer_reduce_gb300 import traffic
     g = json.load(open(GOLDEN, encoding="utf-8"))

@@ -16,11 +16,15 @@
 namespace lsr {
 
 int64_t dgdb_rows_per_chunk(int64_t rows, int64_t hidden) {
+    // At most about 456 blocks (256-column tiles x row chunks): three
+    // resident blocks on each of a GB300's 152 SMs, one wave with no partial
+    // second wave.  A constant, not the device's SM count, so the summation
+    // order depends only on (rows, hidden).
     if (rows <= 0 || hidden <= 0) return 1;
     const int64_t tiles = (hidden + 255) / 256;
-    int64_t target = rows * tiles / 1024;
-    int64_t rpc = 16;
-    while (rpc < 256 && rpc * 2 <= target) rpc *= 2;
+    const int64_t target_chunks = tiles < 456 ? 456 / tiles : 1;
+    int64_t rpc = (rows + target_chunks - 1) / target_chunks;
+    if (rpc < 16) rpc = 16;
     while ((rows + rpc - 1) / rpc > 65535) rpc *= 2;
     return rpc;
 }

@@ -308,7 +308,9 @@ cudaError_t launch_ln_dgdb(float *dgamma, float *dbeta, const T *dy, const T *x,
         if (vec) {
             constexpr int V = Traits<T>::kVec;
             dim3 grid((unsigned)ceil_div(N, 32 * V), (unsigned)nchunks);
-            cudaError_t e = launch_pdl(ln_dgdb_partial<T, V>, grid, dim3(kDgdbWarps * 32), 0, st,
+            constexpr size_t smem = ln_dgdb_staged_smem<T>();
+            ensure_dynamic_smem<ln_dgdb_staged<T>>(smem);
+            cudaError_t e = launch_pdl(ln_dgdb_staged<T>, grid, dim3(kDgdbWarps * 32), smem, st,
                                        part, dy, x, mean, rstd, rows, N, rpc);
             if (e != cudaSuccess) return e;
         } else {

@@ -705,6 +705,131 @@ ln_dgdb_partial(float *part, const T *dy, const T *x, const float *mean,
 }
 
 // ----------------------------------------------------------------------------
+// gamma / beta gradient, stage 1, vectorised: the same partial sums as
+// ln_dgdb_partial (the same tiles, warp-to-row assignment, fp32 arithmetic and
+// warp-order combine), with each warp streaming its rows through a private
+// ring of kDgdbStages cp.async stages of kDgdbRows rows each (512 contiguous
+// bytes of dy and of x per row, plus the rows' mean and rstd), so that
+// (kDgdbStages - 1) * kDgdbRows rows per warp are in flight and the per-stage
+// bookkeeping is shared by kDgdbRows rows.  The ring is reused for the
+// warp-order combine at the end.  mean == nullptr means mean 0 (RMSNorm).
+// ----------------------------------------------------------------------------
+constexpr int kDgdbStages = 4;
+constexpr int kDgdbRows = 2;
+
+template <typename T>
+constexpr size_t ln_dgdb_staged_smem() {
+    return (size_t)kDgdbWarps * kDgdbStages * kDgdbRows * (64 * 16 + 2 * 4);
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kDgdbWarps * 32, 3)
+ln_dgdb_staged(float *part, const T *dy, const T *x, const float *mean, const float *rstd,
+               int64_t rows, int64_t N, int64_t rows_per_chunk) {
+    pdl_begin();
+    using Tr = Traits<T>;
+    constexpr int V = Tr::kVec;
+    constexpr int CT = 32 * V;  // columns per tile
+    constexpr int S = kDgdbStages;
+    constexpr int R = kDgdbRows;
+    static_assert(2 * kDgdbWarps * CT * 4 <= kDgdbWarps * S * R * 64 * 16, "combine fits the ring");
+    extern __shared__ uint4 dsmem[];
+    const int lane = threadIdx.x & 31;
+    const int w = threadIdx.x >> 5;
+    uint4 *ring = dsmem + (size_t)w * S * R * 64;  // [S][R][dy, x][32 lanes]
+    float *stat = reinterpret_cast<float *>(dsmem + kDgdbWarps * S * R * 64) + w * S * R * 2;
+
+    const int64_t col0 = (int64_t)blockIdx.x * CT + lane * V;
+    const bool colok = col0 < N;
+    const int64_t chunk = blockIdx.y;
+    const int64_t r0 = chunk * rows_per_chunk;
+    const int64_t r1 = min(rows, r0 + rows_per_chunk);
+    // this warp's rows: r0 + w + 8 j, j < nk, taken R at a time
+    const int64_t nk = r1 - r0 > w ? (r1 - r0 - w + kDgdbWarps - 1) / kDgdbWarps : 0;
+    const int64_t nst = (nk + R - 1) / R;
+
+    float ag[V], ab[V];
+#pragma unroll
+    for (int e = 0; e < V; ++e) ag[e] = ab[e] = 0.f;
+
+    // running source pointers of the next stage to issue
+    const int64_t rstep = (int64_t)kDgdbWarps * N;
+    const T *pdy = dy + (r0 + w) * N + col0;
+    const T *px = x + (r0 + w) * N + col0;
+    const float *pst = (lane & 1) ? rstd + r0 + w : mean + r0 + w;  // lanes 0..2R-1
+    const bool stat_lane = lane < 2 * R && (mean != nullptr || (lane & 1));
+    int64_t jnext = 0;
+    auto issue = [&](int st) {
+#pragma unroll
+        for (int rr = 0; rr < R; ++rr) {
+            if (jnext + rr < nk) {
+                if (colok) {
+                    cp_async16(&ring[(st * R + rr) * 64 + lane], pdy + rr * rstep);
+                    cp_async16(&ring[(st * R + rr) * 64 + 32 + lane], px + rr * rstep);
+                }
+                if (stat_lane && (lane >> 1) == rr)
+                    cp_async4(&stat[(st * R + rr) * 2 + (lane & 1)], pst + rr * kDgdbWarps);
+            }
+        }
+        jnext += R;
+        pdy += R * rstep;
+        px += R * rstep;
+        pst += R * kDgdbWarps;
+        cp_async_commit();
+    };
+#pragma unroll
+    for (int st = 0; st < S - 1; ++st) issue(st);
+
+    int s_cur = 0, s_iss = S - 1;
+    for (int64_t k = 0; k < nst; ++k) {
+        issue(s_iss);
+        s_iss = s_iss + 1 == S ? 0 : s_iss + 1;
+        cp_async_wait<S - 1>();
+        __syncwarp();  // the statistics lanes' copies are visible to the warp
+#pragma unroll
+        for (int rr = 0; rr < R; ++rr) {
+            if (k * R + rr < nk && colok) {
+                const float mu = mean ? stat[(s_cur * R + rr) * 2] : 0.f;
+                const float rs = stat[(s_cur * R + rr) * 2 + 1];
+                float dv[V], xv[V];
+                Tr::unpack(ring[(s_cur * R + rr) * 64 + lane], dv);
+                Tr::unpack(ring[(s_cur * R + rr) * 64 + 32 + lane], xv);
+#pragma unroll
+                for (int e = 0; e < V; ++e) {
+                    ag[e] = fmaf(dv[e], (xv[e] - mu) * rs, ag[e]);
+                    ab[e] += dv[e];
+                }
+            }
+        }
+        __syncwarp();  // the next issue refills this stage
+        s_cur = s_cur + 1 == S ? 0 : s_cur + 1;
+    }
+
+    __syncthreads();  // every warp is done with its ring (no copy in flight)
+    float *sg = reinterpret_cast<float *>(dsmem);  // [warps][CT]
+    float *sb = sg + kDgdbWarps * CT;              // [warps][CT]
+#pragma unroll
+    for (int e = 0; e < V; ++e) {
+        sg[w * CT + lane * V + e] = ag[e];
+        sb[w * CT + lane * V + e] = ab[e];
+    }
+    __syncthreads();
+    for (int cc = threadIdx.x; cc < CT; cc += kDgdbWarps * 32) {
+        const int64_t col = (int64_t)blockIdx.x * CT + cc;
+        if (col < N) {
+            float a = sg[cc], b = sb[cc];
+#pragma unroll
+            for (int ww = 1; ww < kDgdbWarps; ++ww) {
+                a += sg[ww * CT + cc];
+                b += sb[ww * CT + cc];
+            }
+            part[(chunk * 2 + 0) * N + col] = a;
+            part[(chunk * 2 + 1) * N + col] = b;
+        }
+    }
+}
+
+// ----------------------------------------------------------------------------
 // gamma / beta gradient, stage 2: sum the chunk partials in a fixed order.
 // Block = 32 columns x 32 chunk lanes; chunk lane t sums chunks t, t+32, ...
 // in increasing order, loading a batch of 8 of them at once (the kernel is
