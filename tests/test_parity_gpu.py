@@ -206,6 +206,26 @@ def test_encoder_big_layer_pass_bf16():
         compare(b.dbeta.cpu()[cols], rb, c.dtype, f"{c.name} dbeta")
 
 
+def test_pipelined_passes_deliver_the_plain_pass_outputs():
+    """The end-to-end schedule (two device buffer sets, copies on their own
+    streams) brings back exactly what one plain pass computes."""
+    from transformer_reduce_gb300 import workloads as W
+    from transformer_reduce_gb300.layer_path import LayerReducePath, PipelinedPasses
+    mk = lambda: LayerReducePath(W.GPT2_SMALL["softmax"],  # noqa: E731
+                                 [W.GPT2_SMALL["layernorm"], W.TINY["layernorm"]], device=DEV)
+    a, b = mk(), mk()
+    pipe = PipelinedPasses([a, b])
+    for h in pipe.hout:
+        h.fill_(float("nan"))
+    pipe.run(3)  # the last step runs on buffer set a
+    torch.cuda.synchronize()
+    ref = mk()
+    ref.run()
+    torch.cuda.synchronize()
+    for h, d in zip(pipe.hout, ref._outputs()):
+        assert torch.equal(h, d.cpu())
+
+
 # ----------------------------------------------------------------------------
 # edge cases
 # ----------------------------------------------------------------------------

@@ -191,3 +191,85 @@ class LayerReducePath:
         with torch.cuda.stream(stream):
             for h, d in zip(hout, self._outputs()):
                 h.copy_(d, non_blocking=True)
+
+
+class PipelinedPasses:
+    """Passes fed from pinned host memory with the copies overlapped.
+
+    Two device copies of the pass's buffers (``paths[0]`` and ``paths[1]``);
+    step k uses copy k % 2.  The host-to-device copies, the kernels and the
+    device-to-host copies run on their own streams; each copy direction is
+    split over ``lanes`` streams (tensors dealt out largest first), so that
+    several copy engines work at once.  Events order step k's upload after
+    step k-2's kernels (they read the same input buffers), its kernels after
+    its upload and after step k-2's download (the same output buffers), and
+    its download after its kernels.  In steady state both copy directions and
+    the kernels of neighbouring steps run at the same time.  Every step
+    uploads every input from the same pinned host buffers and downloads every
+    output into one set of pinned host buffers."""
+
+    def __init__(self, paths, lanes: int = 2):
+        assert len(paths) == 2
+        self.paths = paths
+        self.dev = paths[0].device
+        self.hin, self.hout = paths[0].host_buffers()
+        self.s_up = [torch.cuda.Stream(self.dev) for _ in range(lanes)]
+        self.s_run = torch.cuda.Stream(self.dev)
+        self.s_down = [torch.cuda.Stream(self.dev) for _ in range(lanes)]
+        self.in_lane = self._deal([h.numel() * h.element_size() for h in self.hin], lanes)
+        self.out_lane = self._deal([h.numel() * h.element_size() for h in self.hout], lanes)
+
+    @staticmethod
+    def _deal(sizes, lanes):
+        load = [0] * lanes
+        lane_of = [0] * len(sizes)
+        for i in sorted(range(len(sizes)), key=lambda i: -sizes[i]):
+            j = min(range(lanes), key=lambda j: load[j])
+            lane_of[i] = j
+            load[j] += sizes[i]
+        return lane_of
+
+    def _copies(self, streams, lane_of, pairs):
+        done = []
+        for j, st in enumerate(streams):
+            with torch.cuda.stream(st):
+                for i, (dst, src) in enumerate(pairs):
+                    if lane_of[i] == j:
+                        dst.copy_(src, non_blocking=True)
+            e = torch.cuda.Event()
+            e.record(st)
+            done.append(e)
+        return done
+
+    def run(self, steps: int):
+        """Enqueue `steps` passes; returns (start, end) CUDA events around all
+        of them."""
+        up, comp, down = [], [], []
+        start = torch.cuda.Event(enable_timing=True)
+        end = torch.cuda.Event(enable_timing=True)
+        start.record(self.s_run)
+        for st in self.s_up + self.s_down:
+            st.wait_event(start)
+        for k in range(steps):
+            p = self.paths[k % 2]
+            if k >= 2:
+                for st in self.s_up:
+                    st.wait_event(comp[k - 2])
+            up.append(self._copies(self.s_up, self.in_lane, list(zip(p._inputs(), self.hin))))
+            for e in up[k]:
+                self.s_run.wait_event(e)
+            if k >= 2:
+                for e in down[k - 2]:
+                    self.s_run.wait_event(e)
+            p.run(self.s_run)
+            comp.append(torch.cuda.Event())
+            comp[k].record(self.s_run)
+            for st in self.s_down:
+                st.wait_event(comp[k])
+            down.append(self._copies(self.s_down, self.out_lane,
+                                     list(zip(self.hout, p._outputs()))))
+        # the end waits for every stream's last work
+        for e in down[-1]:
+            self.s_run.wait_event(e)
+        end.record(self.s_run)
+        return start, end
