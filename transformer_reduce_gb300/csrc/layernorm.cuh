@@ -748,9 +748,10 @@ ln_dgdb_staged(float *part, const T *dy, const T *x, const float *mean, const fl
     const int64_t nk = r1 - r0 > w ? (r1 - r0 - w + kDgdbWarps - 1) / kDgdbWarps : 0;
     const int64_t nst = (nk + R - 1) / R;
 
-    float ag[V], ab[V];
+    constexpr int H2 = V / 2;
+    float2 ag[H2], ab[H2];
 #pragma unroll
-    for (int e = 0; e < V; ++e) ag[e] = ab[e] = 0.f;
+    for (int h = 0; h < H2; ++h) ag[h] = ab[h] = f2(0.f);
 
     // running source pointers of the next stage to issue
     const int64_t rstep = (int64_t)kDgdbWarps * N;
@@ -789,15 +790,15 @@ ln_dgdb_staged(float *part, const T *dy, const T *x, const float *mean, const fl
 #pragma unroll
         for (int rr = 0; rr < R; ++rr) {
             if (k * R + rr < nk && colok) {
-                const float mu = mean ? stat[(s_cur * R + rr) * 2] : 0.f;
-                const float rs = stat[(s_cur * R + rr) * 2 + 1];
-                float dv[V], xv[V];
-                Tr::unpack(ring[(s_cur * R + rr) * 64 + lane], dv);
-                Tr::unpack(ring[(s_cur * R + rr) * 64 + 32 + lane], xv);
+                const float2 nmu = f2(mean ? -stat[(s_cur * R + rr) * 2] : 0.f);
+                const float2 rs = f2(stat[(s_cur * R + rr) * 2 + 1]);
+                float2 dv[H2], xv[H2];
+                unpack2<T>(ring[(s_cur * R + rr) * 64 + lane], dv);
+                unpack2<T>(ring[(s_cur * R + rr) * 64 + 32 + lane], xv);
 #pragma unroll
-                for (int e = 0; e < V; ++e) {
-                    ag[e] = fmaf(dv[e], (xv[e] - mu) * rs, ag[e]);
-                    ab[e] += dv[e];
+                for (int h = 0; h < H2; ++h) {
+                    ag[h] = fma2(dv[h], mul2(add2(xv[h], nmu), rs), ag[h]);
+                    ab[h] = add2(ab[h], dv[h]);
                 }
             }
         }
@@ -809,9 +810,11 @@ ln_dgdb_staged(float *part, const T *dy, const T *x, const float *mean, const fl
     float *sg = reinterpret_cast<float *>(dsmem);  // [warps][CT]
     float *sb = sg + kDgdbWarps * CT;              // [warps][CT]
 #pragma unroll
-    for (int e = 0; e < V; ++e) {
-        sg[w * CT + lane * V + e] = ag[e];
-        sb[w * CT + lane * V + e] = ab[e];
+    for (int h = 0; h < H2; ++h) {
+        sg[w * CT + lane * V + 2 * h] = ag[h].x;
+        sg[w * CT + lane * V + 2 * h + 1] = ag[h].y;
+        sb[w * CT + lane * V + 2 * h] = ab[h].x;
+        sb[w * CT + lane * V + 2 * h + 1] = ab[h].y;
     }
     __syncthreads();
     for (int cc = threadIdx.x; cc < CT; cc += kDgdbWarps * 32) {

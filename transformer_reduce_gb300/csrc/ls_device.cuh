@@ -147,19 +147,14 @@ __device__ __forceinline__ uint4 pack2<__nv_bfloat16>(const float2 (&f)[4]) {
 }
 __device__ __forceinline__ float2 f2(float a) { return make_float2(a, a); }
 
-// Pair arithmetic, element by element in scalar FP32, each operation rounded
-// to nearest and never contracted into a fused multiply-add (add2, mul2) or
-// fused exactly once (fma2).  Scalar instructions on purpose: every kernel of
-// the library uses only long-established FP32 instructions.
-__device__ __forceinline__ float2 add2(float2 a, float2 b) {
-    return make_float2(__fadd_rn(a.x, b.x), __fadd_rn(a.y, b.y));
-}
-__device__ __forceinline__ float2 mul2(float2 a, float2 b) {
-    return make_float2(__fmul_rn(a.x, b.x), __fmul_rn(a.y, b.y));
-}
-__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
-    return make_float2(__fmaf_rn(a.x, b.x, c.x), __fmaf_rn(a.y, b.y, c.y));
-}
+// Pair arithmetic on Blackwell's packed FP32x2 instructions: two independent
+// FP32 operations per instruction, each rounded to nearest exactly as its
+// scalar form (add2, mul2 are never contracted into a fused multiply-add;
+// fma2 fuses once), so results are bitwise those of scalar code while the
+// issue slots spent on FP32 arithmetic halve.
+__device__ __forceinline__ float2 add2(float2 a, float2 b) { return __fadd2_rn(a, b); }
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) { return __fmul2_rn(a, b); }
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
 
 // ----------------------------------------------------------------------------
 // Programmatic dependent launch (sm_90+).  Every kernel of the library starts
