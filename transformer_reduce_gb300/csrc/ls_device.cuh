@@ -147,6 +147,14 @@ __device__ __forceinline__ uint4 pack2<__nv_bfloat16>(const float2 (&f)[4]) {
 }
 __device__ __forceinline__ float2 f2(float a) { return make_float2(a, a); }
 
+// Maximum of three floats in one instruction (PTX three-input max.f32,
+// sm_100 and later); exact, like two two-input maxima.
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+
 // Pair arithmetic on Blackwell's packed FP32x2 instructions: two independent
 // FP32 operations per instruction, each rounded to nearest exactly as its
 // scalar form (add2, mul2 are never contracted into a fused multiply-add;

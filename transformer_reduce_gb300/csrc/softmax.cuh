@@ -211,7 +211,7 @@ softmax_fw_vec(T *out, const T *inp, const T *mask, int64_t rows,
                     }
                 }
 #pragma unroll
-                for (int h = 0; h < H2; ++h) m = fmaxf(m, fmaxf(v[kk][h].x, v[kk][h].y));
+                for (int h = 0; h < H2; ++h) m = fmax3(m, v[kk][h].x, v[kk][h].y);
             }
         }
         m = group_reduce<TPR, OpMax>(m, red);
