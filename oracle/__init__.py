@@ -71,6 +71,12 @@ def _load():
         lib.ref_softmax_fw_offset.restype = None
         lib.ref_softmax_bw_masked.argtypes = [dp, dp, dp, dp, ip, ip, i64, i64, ctypes.c_int, i64]
         lib.ref_softmax_bw_masked.restype = None
+        lib.ref_softmax_fw_scaled.argtypes = [dp, dp, dp, ip, ip, i64, i64, ctypes.c_int, i64,
+                                              ctypes.c_double]
+        lib.ref_softmax_fw_scaled.restype = None
+        lib.ref_softmax_bw_masked_scaled.argtypes = [dp, dp, dp, dp, ip, ip, i64, i64,
+                                                     ctypes.c_int, i64, ctypes.c_double]
+        lib.ref_softmax_bw_masked_scaled.restype = None
         lib.ref_layernorm_fw.argtypes = [dp, dp, dp, dp, dp, dp, i64, i64,
                                          ctypes.c_double]
         lib.ref_layernorm_fw.restype = None
@@ -217,6 +223,52 @@ def softmax_bw_masked_tensor(dy4, y4, mask=None, causal=False):
     rows = np.arange(B * H * Tq, dtype=np.int64)
     dx = softmax_bw_masked(dy4.reshape(-1, Tk), y4.reshape(-1, Tk), mask, batch=rows // (H * Tq),
                            query=rows % Tq, causal=causal, offset=Tk - Tq)
+    return dx.reshape(B, H, Tq, Tk)
+
+
+def softmax_fw_scaled(x, mask=None, batch=None, query=None, causal=False, offset=0, scale=1.0):
+    """Softmax of scale * x + mask, causal keys visible up to query + offset."""
+    x = _f64(x)
+    nrows, tk = x.shape
+    m = _f64(mask)
+    pb, pq, batch, query = _rows_meta(nrows, m, batch, query, causal)
+    y = np.empty_like(x)
+    _load().ref_softmax_fw_scaled(_ptr(y), _ptr(x), _ptr(m), pb, pq, nrows, tk,
+                                  int(bool(causal)), int(offset), float(scale))
+    return y
+
+
+def softmax_fw_tensor_scaled(x4, mask=None, causal=False, scale=1.0):
+    """Scaled softmax forward of [B,H,Tq,Tk], Tq <= Tk, bottom-right causal."""
+    x4 = _f64(x4)
+    B, H, Tq, Tk = x4.shape
+    rows = np.arange(B * H * Tq, dtype=np.int64)
+    y = softmax_fw_scaled(x4.reshape(-1, Tk), mask, batch=rows // (H * Tq), query=rows % Tq,
+                          causal=causal, offset=Tk - Tq, scale=scale)
+    return y.reshape(B, H, Tq, Tk)
+
+
+def softmax_bw_masked_scaled(dy, y, mask=None, batch=None, query=None, causal=False, offset=0,
+                             scale=1.0):
+    """Backward of the scaled softmax over the visible keys (0 elsewhere)."""
+    dy, y = _f64(dy), _f64(y)
+    assert dy.shape == y.shape
+    nrows, tk = dy.shape
+    m = _f64(mask)
+    pb, pq, batch, query = _rows_meta(nrows, m, batch, query, causal)
+    dx = np.empty_like(dy)
+    _load().ref_softmax_bw_masked_scaled(_ptr(dx), _ptr(dy), _ptr(y), _ptr(m), pb, pq, nrows, tk,
+                                         int(bool(causal)), int(offset), float(scale))
+    return dx
+
+
+def softmax_bw_masked_scaled_tensor(dy4, y4, mask=None, causal=False, scale=1.0):
+    dy4, y4 = _f64(dy4), _f64(y4)
+    B, H, Tq, Tk = dy4.shape
+    rows = np.arange(B * H * Tq, dtype=np.int64)
+    dx = softmax_bw_masked_scaled(dy4.reshape(-1, Tk), y4.reshape(-1, Tk), mask,
+                                  batch=rows // (H * Tq), query=rows % Tq, causal=causal,
+                                  offset=Tk - Tq, scale=scale)
     return dx.reshape(B, H, Tq, Tk)
 
 

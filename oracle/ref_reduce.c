@@ -222,6 +222,74 @@ void ref_softmax_bw_masked(double *dx, const double *dy, const double *y,
     }
 }
 
+/*
+ * Scaled softmax forward (the fused "scale + mask + softmax" of an attention
+ * layer): the scores are multiplied by `scale` (e.g. 1/sqrt(d)) before the
+ * additive mask:
+ *   z_j = -inf                          if causal and j > query[r] + offset
+ *   z_j = scale * x_j + mask[b, j]      otherwise
+ *   y   = exp(z - max z) / sum exp(z - max z)   (zeros when max z = -inf)
+ */
+void ref_softmax_fw_scaled(double *y, const double *x, const double *mask,
+                           const int64_t *batch, const int64_t *query,
+                           int64_t nrows, int64_t Tk, int causal,
+                           int64_t offset, double scale)
+{
+    for (int64_t r = 0; r < nrows; ++r) {
+        const double *xr = x + r * Tk;
+        double *yr = y + r * Tk;
+        const double *mr = mask ? mask + batch[r] * Tk : 0;
+        const int64_t q = causal ? query[r] : 0;
+        double m = -INFINITY;
+        for (int64_t j = 0; j < Tk; ++j) {
+            double z = -INFINITY;
+            if (!(causal && j > q + offset))
+                z = scale * xr[j] + (mr ? mr[j] : 0.0);
+            yr[j] = z;
+            if (z > m)
+                m = z;
+        }
+        if (m == -INFINITY) {
+            for (int64_t j = 0; j < Tk; ++j)
+                yr[j] = 0.0;
+            continue;
+        }
+        double s = 0.0;
+        for (int64_t j = 0; j < Tk; ++j) {
+            yr[j] = exp(yr[j] - m);
+            s += yr[j];
+        }
+        for (int64_t j = 0; j < Tk; ++j)
+            yr[j] /= s;
+    }
+}
+
+/*
+ * Backward of the scaled softmax over the visible keys: with y the forward
+ * output, d z_j / d x_j = scale, so
+ *   s    = sum over visible k of y_k dy_k
+ *   dx_j = scale * y_j * (dy_j - s)   for visible j,   0 otherwise.
+ */
+void ref_softmax_bw_masked_scaled(double *dx, const double *dy, const double *y,
+                                  const double *mask, const int64_t *batch,
+                                  const int64_t *query, int64_t nrows, int64_t Tk,
+                                  int causal, int64_t offset, double scale)
+{
+    for (int64_t r = 0; r < nrows; ++r) {
+        const double *yr = y + r * Tk;
+        const double *dyr = dy + r * Tk;
+        double *dxr = dx + r * Tk;
+        const double *mr = mask ? mask + batch[r] * Tk : 0;
+        const int64_t q = causal ? query[r] : 0;
+        double s = 0.0;
+        for (int64_t k = 0; k < Tk; ++k)
+            if (visible(mr, k, q, offset, causal))
+                s += yr[k] * dyr[k];
+        for (int64_t j = 0; j < Tk; ++j)
+            dxr[j] = visible(mr, j, q, offset, causal) ? scale * yr[j] * (dyr[j] - s) : 0.0;
+    }
+}
+
 /* ------------------------------------------------------------------------ */
 /* LayerNorm forward                                                         */
 /* ------------------------------------------------------------------------ */

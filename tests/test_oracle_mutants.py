@@ -63,6 +63,13 @@ MUTANTS = [
     ("ce_bw_no_dloss", "dzr[j] = dloss[r] * (exp(zr[j] - lse[r])", "dzr[j] = 1.0 * (exp(zr[j] - lse[r])", 0),
     ("ce_bw_out_of_range_kept", "else if ((int64_t)t >= V)\n                dzr[j] = NAN;",
      "else if ((int64_t)t >= V + 1)\n                dzr[j] = NAN;", 0),
+    ("scaled_fw_scale_dropped", "z = scale * xr[j] + (mr ? mr[j] : 0.0);",
+     "z = xr[j] + (mr ? mr[j] : 0.0);", 0),
+    ("scaled_fw_scale_on_mask", "z = scale * xr[j] + (mr ? mr[j] : 0.0);",
+     "z = scale * (xr[j] + (mr ? mr[j] : 0.0));", 0),
+    ("scaled_fw_offset_dropped", "if (!(causal && j > q + offset))", "if (!(causal && j > q))", 0),
+    ("scaled_bw_scale_dropped", "scale * yr[j] * (dyr[j] - s)", "yr[j] * (dyr[j] - s)", 0),
+    ("scaled_bw_scale_squared", "scale * yr[j] * (dyr[j] - s)", "scale * scale * yr[j] * (dyr[j] - s)", 0),
     ("masked_bw_sum_all_keys", "if (visible(mr, k, q, offset, causal))\n                s += yr[k] * dyr[k];",
      "s += yr[k] * dyr[k];", 0),
     ("masked_bw_no_zeroing", "dxr[j] = visible(mr, j, q, offset, causal) ? yr[j] * (dyr[j] - s) : 0.0;",

@@ -585,3 +585,74 @@ def test_cross_entropy_bw_matches_torch_autograd(ref):
     _, lse = ref.cross_entropy_fw(z.detach().numpy(), t.numpy())
     np.testing.assert_allclose(ref.cross_entropy_bw(z.detach().numpy(), t.numpy(), lse, dl.numpy()),
                                z.grad.numpy(), rtol=1e-11, atol=1e-13)
+
+
+# ----------------------------------------------------------------------------
+# scaled softmax (the fused "scale + mask + softmax"): z = scale * x + mask
+# ----------------------------------------------------------------------------
+
+def _torch_scaled_softmax(x4, mask, causal, scale):
+    B, H, Tq, Tk = x4.shape
+    z = scale * x4 + torch.as_tensor(mask).view(B, 1, 1, Tk)
+    if causal:
+        i = torch.arange(Tq).view(Tq, 1)
+        j = torch.arange(Tk).view(1, Tk)
+        z = z.masked_fill(j > i + (Tk - Tq), float("-inf"))
+    return torch.softmax(z, dim=-1)
+
+
+@pytest.mark.parametrize("causal,Tq,Tk", [(False, 7, 7), (True, 5, 9), (True, 6, 6)])
+def test_scaled_softmax_matches_torch_autograd(ref, causal, Tq, Tk):
+    rng = np.random.default_rng(91)
+    B, H, scale = 2, 3, 0.125
+    x = torch.tensor(rng.normal(0, 3, size=(B, H, Tq, Tk)), requires_grad=True)
+    mask = rng.normal(0, 1, size=(B, Tk))  # a non-binary additive bias
+    mask[0, Tk - 2:] = -np.inf
+    dy = torch.tensor(rng.normal(size=(B, H, Tq, Tk)))
+    yt = _torch_scaled_softmax(x, mask, causal, scale)
+    yt.backward(dy)
+    y = ref.softmax_fw_tensor_scaled(x.detach().numpy(), mask, causal=causal, scale=scale)
+    np.testing.assert_allclose(y, yt.detach().numpy(), rtol=1e-12, atol=1e-15)
+    dx = ref.softmax_bw_masked_scaled_tensor(dy.numpy(), y, mask, causal=causal, scale=scale)
+    np.testing.assert_allclose(dx, x.grad.numpy(), rtol=1e-10, atol=1e-13)
+
+
+def test_scaled_softmax_reduces_to_the_unscaled_one(ref):
+    rng = np.random.default_rng(92)
+    x = rng.normal(0, 2, size=(4, 2, 6, 10))
+    mask = _padding_mask([7, 10, 3, 9], 10)
+    # scale 2: z = 2x + mask exactly, the unscaled softmax of 2x
+    y2 = ref.softmax_fw_tensor_scaled(x, mask, causal=True, scale=2.0)
+    assert np.array_equal(y2, ref.softmax_fw_tensor_offset(2.0 * x, mask, causal=True))
+    y1 = ref.softmax_fw_tensor_scaled(x, mask, causal=True, scale=1.0)
+    dy = rng.normal(size=x.shape)
+    assert np.array_equal(ref.softmax_bw_masked_scaled_tensor(dy, y1, mask, causal=True, scale=1.0),
+                          ref.softmax_bw_masked_tensor(dy, y1, mask, causal=True))
+    # scale 0.5 on the backward is half the unscaled backward, exactly
+    assert np.array_equal(ref.softmax_bw_masked_scaled_tensor(dy, y1, mask, causal=True, scale=0.5),
+                          0.5 * ref.softmax_bw_masked_tensor(dy, y1, mask, causal=True))
+
+
+def test_scaled_softmax_bw_central_differences(ref):
+    rng = np.random.default_rng(93)
+    B, H, Tq, Tk, scale = 1, 2, 3, 5, 0.35
+    x = rng.normal(0, 1.5, size=(B, H, Tq, Tk))
+    mask = np.array([[0.0, 0.5, -np.inf, -0.25, 0.0]])
+    dy = rng.normal(size=x.shape)
+
+    def loss(xx):
+        return float(np.sum(dy * ref.softmax_fw_tensor_scaled(xx, mask, causal=True, scale=scale)))
+
+    y = ref.softmax_fw_tensor_scaled(x, mask, causal=True, scale=scale)
+    dx = ref.softmax_bw_masked_scaled_tensor(dy, y, mask, causal=True, scale=scale)
+    h = 1e-6
+    fd = np.zeros_like(x)
+    for idx in np.ndindex(x.shape):
+        xp, xm = x.copy(), x.copy()
+        xp[idx] += h
+        xm[idx] -= h
+        fd[idx] = (loss(xp) - loss(xm)) / (2 * h)
+    assert np.max(np.abs(dx - fd)) <= 1e-7
+    # masked key 2 and (bottom-right causal, offset 2) keys j > i + 2 are exactly 0
+    assert np.all(y[..., 2] == 0) and np.all(dx[..., 2] == 0)
+    assert np.all(y[:, :, 0, 3:] == 0) and np.all(y[:, :, 1, 4:] == 0)
