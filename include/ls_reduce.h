@@ -127,6 +127,35 @@ ls_status ls_softmax_bw_masked(void *dinp, const void *dout, const void *out_fw,
                                int64_t Tk, int causal, ls_dtype dt, void *stream);
 
 /*
+ * Scaled softmax, forward: the fused "scale + mask + softmax" of an attention
+ * layer (the L10 page, section "Technique 1", fuses the operations between
+ * the GEMMs into custom kernels; the score scale is one of them).  As
+ * ls_softmax_fw, with the scores multiplied by `scale` (e.g. 1/sqrt(head
+ * dimension)) before the additive mask:
+ *     z_j = scale * x_j + mask[b, j]   (-inf for causal future keys)
+ *     y   = softmax(z)
+ * The scale is folded into the exponent (no extra pass, no extra arithmetic
+ * on unmasked chunks).  scale must be finite and > 0, else
+ * LS_ERR_INVALID_ARG.  Other arguments and errors as for ls_softmax_fw;
+ * ls_softmax_fw is this function with scale = 1 (bitwise).
+ */
+ls_status ls_softmax_fw_scaled(void *out, const void *inp, const void *mask, int64_t B,
+                               int64_t H, int64_t Tq, int64_t Tk, int causal, float scale,
+                               ls_dtype dt, void *stream);
+
+/*
+ * Scaled softmax, backward over the visible keys: the gradient of the scores
+ * of ls_softmax_fw_scaled,
+ *     dinp_j = scale * y_j * (dout_j - sum over visible k of y_k dout_k)
+ * on visible keys and 0 on the others (as ls_softmax_bw_masked, which is this
+ * function with scale = 1, bitwise).  scale must be finite and > 0.
+ */
+ls_status ls_softmax_bw_masked_scaled(void *dinp, const void *dout, const void *out_fw,
+                                      const void *mask, int64_t B, int64_t H, int64_t Tq,
+                                      int64_t Tk, int causal, float scale, ls_dtype dt,
+                                      void *stream);
+
+/*
  * LayerNorm forward ("Problem 2.1" of the HW4 page; slide 21 of the L10
  * page).  For every row of x [rows, hidden], the mean and variance come from
  * ONE fused reduction of the two sums sum(x') and sum(x'^2), x' = x - x_0

@@ -96,6 +96,15 @@ def test_rejections_before_launch(abi):
     assert abi.ls_rmsnorm_fw(None, None, None, None, 0, 8, 1e-6, F32) == abi.LS_OK
     assert abi.ls_rmsnorm_bw_dinp(fake, fake, fake, fake, fake + 2, 4, 8, F32) == abi.LS_ERR_MISALIGNED
     assert abi.ls_rmsnorm_bw_dgamma(fake, fake, fake, fake, 16384, 1024, None, 0, BF16) == abi.LS_ERR_WORKSPACE
+    # scaled softmax: the scale must be finite and > 0
+    for bad in (0.0, -0.5, math.inf, math.nan):
+        assert abi.ls_softmax_fw_scaled(fake, fake, None, 1, 1, 4, 4, 0, bad, F32) == abi.LS_ERR_INVALID_ARG
+        assert abi.ls_softmax_bw_masked_scaled(fake, fake, fake, None, 1, 1, 4, 4, 0, bad,
+                                               F32) == abi.LS_ERR_INVALID_ARG
+    assert abi.ls_softmax_fw_scaled(fake, fake, None, 1, 1, 4, 4, 0, 0.5, 9) == abi.LS_ERR_UNSUPPORTED
+    assert abi.ls_softmax_fw_scaled(fake, fake, None, 1, 1, 5, 4, 1, 0.5, F32) == abi.LS_ERR_INVALID_ARG
+    assert abi.ls_softmax_fw_scaled(None, None, None, 0, 1, 4, 4, 0, 0.5, BF16) == abi.LS_OK
+    assert abi.ls_softmax_bw_masked_scaled(None, None, None, None, 0, 1, 4, 4, 1, 0.5, BF16) == abi.LS_OK
     # cross entropy
     assert abi.ls_cross_entropy_fw(fake, fake, fake, fake, 4, 0, F32) == abi.LS_ERR_INVALID_ARG
     assert abi.ls_cross_entropy_fw(fake, fake, fake, fake, -1, 9, F32) == abi.LS_ERR_INVALID_ARG

@@ -519,6 +519,59 @@ def test_softmax_bw_masked_encoder_big_sampled():
 
 
 # ----------------------------------------------------------------------------
+# scaled softmax: softmax(scale * scores + mask) and its masked backward
+# ----------------------------------------------------------------------------
+
+@pytest.mark.parametrize("dtype", ["f32", "f16", "bf16"])
+@pytest.mark.parametrize("shape,lengths,causal,scale", [
+    ((2, 3, 16, 16), [9, 16], True, 0.125),
+    ((2, 3, 16, 256), [200, 77], False, 1 / math.sqrt(64)),
+    ((2, 2, 40, 64), [64, 33], True, 0.3),       # bottom-right causal, Tq < Tk
+    ((1, 2, 8, 100), [61], True, 0.125),         # ragged: looped path
+    ((1, 1, 3, 5000), [4000], False, 0.05),      # beyond the register buckets
+])
+def test_scaled_softmax_forward_and_masked_backward(dtype, shape, lengths, causal, scale):
+    L = _L()
+    B, H, Tq, Tk = shape
+    x, dout, mask = _rand_problem(B, H, Tq, Tk, dtype, 71, lengths)
+    # a non-binary additive bias on the valid keys, -inf on the padding
+    g = torch.Generator(device=DEV).manual_seed(72)
+    bias = torch.randn(B, Tk, generator=g, device=DEV).to(mask.dtype)
+    mask = torch.where(torch.isinf(mask.float()), mask, bias)
+    y = L.softmax_fw(x, mask, causal=causal, scale=scale)
+    torch.cuda.synchronize()
+    ref = oracle.softmax_fw_tensor_scaled(x.cpu(), mask.cpu(), causal=causal, scale=scale)
+    compare(y, ref, dtype, f"scaled fw {shape}")
+    assert np.all(y.cpu().float().numpy()[ref == 0.0] == 0.0)
+    yin = torch.from_numpy(ref).to(_dt(dtype)).to(DEV)
+    dx = L.softmax_bw_masked(dout, yin, mask, causal=causal, scale=scale)
+    torch.cuda.synchronize()
+    want = oracle.softmax_bw_masked_scaled_tensor(dout.cpu(), yin.cpu(), mask.cpu(),
+                                                  causal=causal, scale=scale)
+    compare(dx, want, dtype, f"scaled masked bw {shape}")
+    # scale 1 is the unscaled entry point, bit for bit
+    assert torch.equal(L.softmax_fw(x, mask, causal=causal, scale=1.0),
+                       L.softmax_fw(x, mask, causal=causal))
+    assert torch.equal(L.softmax_bw_masked(dout, yin, mask, causal=causal, scale=1.0),
+                       L.softmax_bw_masked(dout, yin, mask, causal=causal))
+
+
+def test_scaled_softmax_encoder_big_sampled():
+    """The Transformer-big encoder shape with the 1/sqrt(64) score scale."""
+    L = _L()
+    from transformer_reduce_gb300 import workloads as W
+    s = W.ENCODER_BIG["softmax"]
+    inp = W.softmax_inputs(s, device=DEV)
+    scale = 0.125
+    y = L.softmax_fw(inp["scores"], inp["mask"], scale=scale)
+    torch.cuda.synchronize()
+    rows = sample_rows(s.rows, boundaries=[b * s.H * s.T for b in range(1, s.B)], seed=9)
+    xr = take_rows(inp["scores"], rows)
+    ref = oracle.softmax_fw_scaled(xr, inp["mask"].cpu(), batch=rows // (s.H * s.T), scale=scale)
+    compare(take_rows(y, rows), ref, s.dtype, "encoder scaled fw")
+
+
+# ----------------------------------------------------------------------------
 # RMSNorm (FastTransformer page, section 5.4)
 # ----------------------------------------------------------------------------
 

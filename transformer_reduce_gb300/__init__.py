@@ -10,7 +10,8 @@ if the library is missing or a call fails, they raise.
 """
 from __future__ import annotations
 
-from ._lib import (LS_BF16, LS_ERR_CUDA, ls_cross_entropy_bw, ls_cross_entropy_fw, LS_ERR_INVALID_ARG, LS_ERR_MISALIGNED,  # noqa: F401
+from ._lib import (LS_BF16, LS_ERR_CUDA, ls_cross_entropy_bw, ls_cross_entropy_fw,
+                   ls_softmax_bw_masked_scaled, ls_softmax_fw_scaled, LS_ERR_INVALID_ARG, LS_ERR_MISALIGNED,  # noqa: F401
                    LS_ERR_UNSUPPORTED, LS_ERR_WORKSPACE, LS_F16, LS_F32, LS_OK, LsError,
                    ls_layernorm_bw_dgamma_dbeta, ls_layernorm_bw_dgamma_dbeta_workspace_size,
                    ls_layernorm_bw, ls_layernorm_bw_dinp, ls_layernorm_bw_workspace_size,
@@ -22,7 +23,8 @@ __all__ = [
     "softmax_fw", "softmax_bw", "softmax_bw_masked", "layernorm_fw", "layernorm_bw_dinp",
     "layernorm_bw_dgamma_dbeta", "dgamma_dbeta_workspace", "layernorm_bw", "rmsnorm_fw", "rmsnorm_bw_dinp",
     "rmsnorm_bw_dgamma", "cross_entropy_fw", "cross_entropy_bw", "LsError", "load",
-    "ls_cross_entropy_fw", "ls_cross_entropy_bw",
+    "ls_cross_entropy_fw", "ls_cross_entropy_bw", "ls_softmax_fw_scaled",
+    "ls_softmax_bw_masked_scaled",
     "ls_softmax_fw", "ls_softmax_bw", "ls_softmax_bw_masked", "ls_layernorm_fw", "ls_layernorm_bw_dinp",
     "ls_layernorm_bw_dgamma_dbeta", "ls_layernorm_bw_dgamma_dbeta_workspace_size",
     "ls_layernorm_bw", "ls_layernorm_bw_workspace_size", "ls_rmsnorm_fw", "ls_rmsnorm_bw_dinp", "ls_rmsnorm_bw_dgamma",
@@ -66,10 +68,11 @@ def _ok(status: int, where: str):
         raise LsError(status, where)
 
 
-def softmax_fw(scores, mask=None, causal: bool = False, out=None):
-    """Softmax over the last axis of scores [B,H,Tq,Tk] plus an additive mask
-    [B,Tk] (broadcast over heads and queries), future keys j > i + Tk - Tq
-    masked when ``causal`` (Tq <= Tk).  ``out`` may be ``scores`` (in place)."""
+def softmax_fw(scores, mask=None, causal: bool = False, out=None, scale=None):
+    """Softmax over the last axis of scale * scores [B,H,Tq,Tk] plus an
+    additive mask [B,Tk] (broadcast over heads and queries), future keys
+    j > i + Tk - Tq masked when ``causal`` (Tq <= Tk).  ``scale`` None is 1.
+    ``out`` may be ``scores`` (in place)."""
     torch = _torch()
     if scores.dim() != 4:
         raise ValueError("scores must be [B, H, Tq, Tk]")
@@ -78,8 +81,13 @@ def softmax_fw(scores, mask=None, causal: bool = False, out=None):
         raise ValueError("mask must be [B, Tk] with the scores' dtype")
     out = torch.empty_like(scores) if out is None else out
     _dev(scores, mask, out)
-    _ok(ls_softmax_fw(_ptr(out), _ptr(scores), _ptr(mask), B, H, Tq, Tk, causal,
-                      ls_dtype(scores), _stream(scores)), "ls_softmax_fw")
+    if scale is None:
+        _ok(ls_softmax_fw(_ptr(out), _ptr(scores), _ptr(mask), B, H, Tq, Tk, causal,
+                          ls_dtype(scores), _stream(scores)), "ls_softmax_fw")
+    else:
+        _ok(ls_softmax_fw_scaled(_ptr(out), _ptr(scores), _ptr(mask), B, H, Tq, Tk, causal,
+                                 float(scale), ls_dtype(scores), _stream(scores)),
+            "ls_softmax_fw_scaled")
     return out
 
 
@@ -97,9 +105,10 @@ def softmax_bw(dout, out_fw, dinp=None):
     return dinp
 
 
-def softmax_bw_masked(dout, out_fw, mask=None, causal: bool = False, dinp=None):
+def softmax_bw_masked(dout, out_fw, mask=None, causal: bool = False, dinp=None, scale=None):
     """Softmax backward that reads only visible keys (mask != -inf, not in the
-    causal future) and writes 0 on the others."""
+    causal future) and writes 0 on the others; with ``scale`` the gradient of
+    the scores of ``softmax_fw(..., scale=scale)``."""
     torch = _torch()
     if dout.dim() != 4 or dout.shape != out_fw.shape or dout.dtype != out_fw.dtype:
         raise ValueError("dout and out_fw must be [B, H, Tq, Tk] of one dtype")
@@ -108,8 +117,13 @@ def softmax_bw_masked(dout, out_fw, mask=None, causal: bool = False, dinp=None):
         raise ValueError("mask must be [B, Tk] with the gradients' dtype")
     dinp = torch.empty_like(dout) if dinp is None else dinp
     _dev(dout, out_fw, mask, dinp)
-    _ok(ls_softmax_bw_masked(_ptr(dinp), _ptr(dout), _ptr(out_fw), _ptr(mask), B, H, Tq, Tk,
-                             causal, ls_dtype(dout), _stream(dout)), "ls_softmax_bw_masked")
+    if scale is None:
+        _ok(ls_softmax_bw_masked(_ptr(dinp), _ptr(dout), _ptr(out_fw), _ptr(mask), B, H, Tq, Tk,
+                                 causal, ls_dtype(dout), _stream(dout)), "ls_softmax_bw_masked")
+    else:
+        _ok(ls_softmax_bw_masked_scaled(_ptr(dinp), _ptr(dout), _ptr(out_fw), _ptr(mask), B, H,
+                                        Tq, Tk, causal, float(scale), ls_dtype(dout),
+                                        _stream(dout)), "ls_softmax_bw_masked_scaled")
     return dinp
 
 

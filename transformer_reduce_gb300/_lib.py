@@ -27,6 +27,9 @@ SIGNATURES = {
     "ls_softmax_fw": ([_VP, _VP, _VP, _I64, _I64, _I64, _I64, _INT, _INT, _VP], _INT),
     "ls_softmax_bw": ([_VP, _VP, _VP, _I64, _I64, _I64, _I64, _INT, _VP], _INT),
     "ls_softmax_bw_masked": ([_VP, _VP, _VP, _VP, _I64, _I64, _I64, _I64, _INT, _INT, _VP], _INT),
+    "ls_softmax_fw_scaled": ([_VP, _VP, _VP, _I64, _I64, _I64, _I64, _INT, _F32, _INT, _VP], _INT),
+    "ls_softmax_bw_masked_scaled": ([_VP, _VP, _VP, _VP, _I64, _I64, _I64, _I64, _INT, _F32, _INT,
+                                     _VP], _INT),
     "ls_layernorm_fw": ([_VP, _VP, _VP, _VP, _VP, _VP, _I64, _I64, _F32, _INT, _VP], _INT),
     "ls_layernorm_bw_dinp": ([_VP, _VP, _VP, _VP, _VP, _VP, _I64, _I64, _INT, _VP], _INT),
     "ls_layernorm_bw_dgamma_dbeta_workspace_size": ([_I64, _I64], _SZ),
@@ -148,3 +151,13 @@ def ls_cross_entropy_fw(loss, lse, logits, target, rows, vocab, dt, stream=0) ->
 
 def ls_cross_entropy_bw(dlogits, logits, target, lse, dloss, rows, vocab, dt, stream=0) -> int:
     return load().ls_cross_entropy_bw(dlogits, logits, target, lse, dloss, rows, vocab, dt, stream)
+
+
+def ls_softmax_fw_scaled(out, inp, mask, B, H, Tq, Tk, causal, scale, dt, stream=0) -> int:
+    return load().ls_softmax_fw_scaled(out, inp, mask, B, H, Tq, Tk, causal, scale, dt, stream)
+
+
+def ls_softmax_bw_masked_scaled(dinp, dout, out_fw, mask, B, H, Tq, Tk, causal, scale, dt,
+                                stream=0) -> int:
+    return load().ls_softmax_bw_masked_scaled(dinp, dout, out_fw, mask, B, H, Tq, Tk, causal,
+                                              scale, dt, stream)

@@ -101,8 +101,9 @@ const char *ls_status_string(ls_status s) {
     return "unknown ls_status";
 }
 
-ls_status ls_softmax_fw(void *out, const void *inp, const void *mask, int64_t B, int64_t H,
-                        int64_t Tq, int64_t Tk, int causal, ls_dtype dt, void *stream) {
+static ls_status softmax_fw_impl(void *out, const void *inp, const void *mask, int64_t B,
+                                 int64_t H, int64_t Tq, int64_t Tk, int causal, float scale,
+                                 ls_dtype dt, void *stream) {
     const size_t es = elem_size(dt);
     if (es == 0) return LS_ERR_UNSUPPORTED;
     if (B < 0 || H < 0 || Tq < 0 || Tk < 0) return LS_ERR_INVALID_ARG;
@@ -121,17 +122,32 @@ ls_status ls_softmax_fw(void *out, const void *inp, const void *mask, int64_t B,
         case LS_F32:
             return from_cuda(lsr::launch_softmax_fw<float>(
                 (float *)out, (const float *)inp, (const float *)mask, rows, H * Tq, Tq, Tk,
-                causal ? 1 : 0, Tk - Tq, vec, st));
+                causal ? 1 : 0, Tk - Tq, scale, vec, st));
         case LS_F16:
             return from_cuda(lsr::launch_softmax_fw<__half>(
                 (__half *)out, (const __half *)inp, (const __half *)mask, rows, H * Tq, Tq, Tk,
-                causal ? 1 : 0, Tk - Tq, vec, st));
+                causal ? 1 : 0, Tk - Tq, scale, vec, st));
         case LS_BF16:
             return from_cuda(lsr::launch_softmax_fw<__nv_bfloat16>(
                 (__nv_bfloat16 *)out, (const __nv_bfloat16 *)inp, (const __nv_bfloat16 *)mask,
-                rows, H * Tq, Tq, Tk, causal ? 1 : 0, Tk - Tq, vec, st));
+                rows, H * Tq, Tq, Tk, causal ? 1 : 0, Tk - Tq, scale, vec, st));
     }
     return LS_ERR_UNSUPPORTED;
+}
+
+static bool scale_ok(float scale) { return std::isfinite(scale) && scale > 0.f; }
+
+ls_status ls_softmax_fw(void *out, const void *inp, const void *mask, int64_t B, int64_t H,
+                        int64_t Tq, int64_t Tk, int causal, ls_dtype dt, void *stream) {
+    return softmax_fw_impl(out, inp, mask, B, H, Tq, Tk, causal, 1.0f, dt, stream);
+}
+
+ls_status ls_softmax_fw_scaled(void *out, const void *inp, const void *mask, int64_t B,
+                               int64_t H, int64_t Tq, int64_t Tk, int causal, float scale,
+                               ls_dtype dt, void *stream) {
+    if (elem_size(dt) == 0) return LS_ERR_UNSUPPORTED;
+    if (!scale_ok(scale)) return LS_ERR_INVALID_ARG;
+    return softmax_fw_impl(out, inp, mask, B, H, Tq, Tk, causal, scale, dt, stream);
 }
 
 ls_status ls_softmax_bw(void *dinp, const void *dout, const void *out_fw, int64_t B, int64_t H,
@@ -164,9 +180,10 @@ ls_status ls_softmax_bw(void *dinp, const void *dout, const void *out_fw, int64_
     return LS_ERR_UNSUPPORTED;
 }
 
-ls_status ls_softmax_bw_masked(void *dinp, const void *dout, const void *out_fw,
-                               const void *mask, int64_t B, int64_t H, int64_t Tq, int64_t Tk,
-                               int causal, ls_dtype dt, void *stream) {
+static ls_status softmax_bw_masked_impl(void *dinp, const void *dout, const void *out_fw,
+                                        const void *mask, int64_t B, int64_t H, int64_t Tq,
+                                        int64_t Tk, int causal, float scale, ls_dtype dt,
+                                        void *stream) {
     const size_t es = elem_size(dt);
     if (es == 0) return LS_ERR_UNSUPPORTED;
     if (B < 0 || H < 0 || Tq < 0 || Tk < 0) return LS_ERR_INVALID_ARG;
@@ -187,18 +204,35 @@ ls_status ls_softmax_bw_masked(void *dinp, const void *dout, const void *out_fw,
         case LS_F32:
             return from_cuda(lsr::launch_softmax_bw_masked<float>(
                 (float *)dinp, (const float *)dout, (const float *)out_fw, (const float *)mask,
-                rows, H * Tq, Tq, Tk, c, Tk - Tq, vec, st));
+                rows, H * Tq, Tq, Tk, c, Tk - Tq, scale, vec, st));
         case LS_F16:
             return from_cuda(lsr::launch_softmax_bw_masked<__half>(
                 (__half *)dinp, (const __half *)dout, (const __half *)out_fw,
-                (const __half *)mask, rows, H * Tq, Tq, Tk, c, Tk - Tq, vec, st));
+                (const __half *)mask, rows, H * Tq, Tq, Tk, c, Tk - Tq, scale, vec, st));
         case LS_BF16:
             return from_cuda(lsr::launch_softmax_bw_masked<__nv_bfloat16>(
                 (__nv_bfloat16 *)dinp, (const __nv_bfloat16 *)dout,
                 (const __nv_bfloat16 *)out_fw, (const __nv_bfloat16 *)mask, rows, H * Tq, Tq,
-                Tk, c, Tk - Tq, vec, st));
+                Tk, c, Tk - Tq, scale, vec, st));
     }
     return LS_ERR_UNSUPPORTED;
+}
+
+ls_status ls_softmax_bw_masked(void *dinp, const void *dout, const void *out_fw,
+                               const void *mask, int64_t B, int64_t H, int64_t Tq, int64_t Tk,
+                               int causal, ls_dtype dt, void *stream) {
+    return softmax_bw_masked_impl(dinp, dout, out_fw, mask, B, H, Tq, Tk, causal, 1.0f, dt,
+                                  stream);
+}
+
+ls_status ls_softmax_bw_masked_scaled(void *dinp, const void *dout, const void *out_fw,
+                                      const void *mask, int64_t B, int64_t H, int64_t Tq,
+                                      int64_t Tk, int causal, float scale, ls_dtype dt,
+                                      void *stream) {
+    if (elem_size(dt) == 0) return LS_ERR_UNSUPPORTED;
+    if (!scale_ok(scale)) return LS_ERR_INVALID_ARG;
+    return softmax_bw_masked_impl(dinp, dout, out_fw, mask, B, H, Tq, Tk, causal, scale, dt,
+                                  stream);
 }
 
 // Shared checks of the LayerNorm entry points.

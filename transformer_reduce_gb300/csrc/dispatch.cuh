@@ -157,25 +157,32 @@ constexpr int kLnDinpStages = 3;
 template <typename T>
 cudaError_t launch_softmax_fw(T *out, const T *inp, const T *mask, int64_t rows,
                               int64_t rows_per_batch, int64_t Tq, int64_t Tk,
-                              int causal, int64_t qoff, bool vec, cudaStream_t st) {
+                              int causal, int64_t qoff, float scale, bool vec, cudaStream_t st) {
     constexpr int V = Traits<T>::kVec;
     int tpr = 0, cpt = 0;
     if (vec && pick_bucket_dense(Tk / V, kSoftmaxFwMaxCpt, kSoftmaxFwMaxTpr, &tpr, &cpt)) {
 #define X(TPR_, CPT_)                                                                   \
-    if (tpr == TPR_ && cpt == CPT_)                                                     \
-        return launch_persistent<softmax_fw_vec<T, TPR_, CPT_, kSoftmaxFwStages>>(      \
+    if (tpr == TPR_ && cpt == CPT_) {                                                   \
+        if (scale == 1.0f)                                                              \
+            return launch_persistent<softmax_fw_vec<T, TPR_, CPT_, kSoftmaxFwStages, false>>( \
+                block_threads<TPR_>(), softmax_fw_smem<TPR_, CPT_, kSoftmaxFwStages>(),    \
+                ceil_div(rows, rows_per_block<TPR_>()), st, out, inp, mask, rows,           \
+                rows_per_batch, Tq, (int)Tk, causal, qoff, scale);                          \
+        return launch_persistent<softmax_fw_vec<T, TPR_, CPT_, kSoftmaxFwStages, true>>(  \
             block_threads<TPR_>(), softmax_fw_smem<TPR_, CPT_, kSoftmaxFwStages>(),        \
             ceil_div(rows, rows_per_block<TPR_>()), st, out, inp, mask, rows,               \
-            rows_per_batch, Tq, (int)Tk, causal, qoff);
+            rows_per_batch, Tq, (int)Tk, causal, qoff, scale);                              \
+    }
         LSR_SOFTMAX_FW_BUCKETS(X)
 #undef X
     }
     if (Tk <= kLoopWarpRowMax)
         return launch_persistent<softmax_fw_loop<T, 32>>(256, 0, ceil_div(rows, 8), st, out, inp,
                                                          mask, rows, rows_per_batch, Tq, Tk,
-                                                         causal, qoff);
+                                                         causal, qoff, scale);
     return launch_persistent<softmax_fw_loop<T, 256>>(256, 0, rows, st, out, inp, mask, rows,
-                                                      rows_per_batch, Tq, Tk, causal, qoff);
+                                                      rows_per_batch, Tq, Tk, causal, qoff,
+                                                      scale);
 }
 
 template <typename T>
@@ -201,7 +208,7 @@ cudaError_t launch_softmax_bw(T *dinp, const T *dout, const T *y, int64_t rows,
 template <typename T>
 cudaError_t launch_softmax_bw_masked(T *dinp, const T *dout, const T *y, const T *mask,
                                      int64_t rows, int64_t rows_per_batch, int64_t Tq,
-                                     int64_t Tk, int causal, int64_t qoff, bool vec,
+                                     int64_t Tk, int causal, int64_t qoff, float scale, bool vec,
                                      cudaStream_t st) {
     constexpr int V = Traits<T>::kVec;
     int tpr = 0, cpt = 0;
@@ -210,16 +217,16 @@ cudaError_t launch_softmax_bw_masked(T *dinp, const T *dout, const T *y, const T
     if (tpr == TPR_ && cpt == CPT_)                                                     \
         return launch_persistent<softmax_bw_masked_vec<T, TPR_, CPT_>>(                 \
             block_threads<TPR_>(), 0, ceil_div(rows, rows_per_block<TPR_>()), st, dinp,     \
-            dout, y, mask, rows, rows_per_batch, Tq, (int)Tk, causal, qoff);
+            dout, y, mask, rows, rows_per_batch, Tq, (int)Tk, causal, qoff, scale);
         LSR_SOFTMAX_BW_BUCKETS(X)
 #undef X
     }
     if (Tk <= kLoopWarpRowMax)
         return launch_persistent<softmax_bw_masked_loop<T, 32>>(
             256, 0, ceil_div(rows, 8), st, dinp, dout, y, mask, rows, rows_per_batch, Tq, Tk,
-            causal, qoff);
+            causal, qoff, scale);
     return launch_persistent<softmax_bw_masked_loop<T, 256>>(
-        256, 0, rows, st, dinp, dout, y, mask, rows, rows_per_batch, Tq, Tk, causal, qoff);
+        256, 0, rows, st, dinp, dout, y, mask, rows, rows_per_batch, Tq, Tk, causal, qoff, scale);
 }
 
 // ----------------------------------------------------------------------------
@@ -378,11 +385,11 @@ cudaError_t launch_rms_dgamma(float *dgamma, const T *dy, const T *x, const floa
 
 #define LSR_INSTANTIATE(T)                                                                      \
     template cudaError_t launch_softmax_fw<T>(T *, const T *, const T *, int64_t, int64_t,     \
-                                              int64_t, int64_t, int, int64_t, bool,            \
+                                              int64_t, int64_t, int, int64_t, float, bool,     \
                                               cudaStream_t);                                   \
     template cudaError_t launch_softmax_bw_masked<T>(T *, const T *, const T *, const T *,     \
                                                      int64_t, int64_t, int64_t, int64_t, int,  \
-                                                     int64_t, bool, cudaStream_t);             \
+                                                     int64_t, float, bool, cudaStream_t);      \
     template cudaError_t launch_softmax_bw<T>(T *, const T *, const T *, int64_t, int64_t,     \
                                               bool, cudaStream_t);                             \
     template cudaError_t launch_ln_fw<T>(T *, float *, float *, const T *, const T *,          \

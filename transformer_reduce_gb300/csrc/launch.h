@@ -19,15 +19,16 @@ int64_t dgdb_num_chunks(int64_t rows, int64_t hidden);
 // Number of SMs of the current device (cached per device).
 int device_sm_count();
 
-// qoff = Tk - Tq: a causal row sees keys j <= (query index) + qoff.
+// qoff = Tk - Tq: a causal row sees keys j <= (query index) + qoff.  scale
+// (> 0) multiplies the scores before the mask is added (1 for plain softmax).
 template <typename T>
 cudaError_t launch_softmax_fw(T *out, const T *inp, const T *mask, int64_t rows,
                               int64_t rows_per_batch, int64_t Tq, int64_t Tk,
-                              int causal, int64_t qoff, bool vec, cudaStream_t st);
+                              int causal, int64_t qoff, float scale, bool vec, cudaStream_t st);
 template <typename T>
 cudaError_t launch_softmax_bw_masked(T *dinp, const T *dout, const T *y, const T *mask,
                                      int64_t rows, int64_t rows_per_batch, int64_t Tq,
-                                     int64_t Tk, int causal, int64_t qoff, bool vec,
+                                     int64_t Tk, int causal, int64_t qoff, float scale, bool vec,
                                      cudaStream_t st);
 template <typename T>
 cudaError_t launch_softmax_bw(T *dinp, const T *dout, const T *y, int64_t rows,

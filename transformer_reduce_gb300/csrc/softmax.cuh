@@ -126,10 +126,11 @@ constexpr size_t softmax_fw_smem() {
     return (size_t)S * (TPR <= 32 ? 256 : TPR) * (CPT * 16 + 4);
 }
 
-template <typename T, int TPR, int CPT, int S>
+template <typename T, int TPR, int CPT, int S, bool SCALED>
 __global__ void __launch_bounds__(TPR <= 32 ? 256 : TPR, (softmax_fw_min_blocks<TPR, CPT>()))
 softmax_fw_vec(T *out, const T *inp, const T *mask, int64_t rows,
-               int64_t rows_per_batch, int64_t Tq, int Tk, int causal, int64_t qoff) {
+               int64_t rows_per_batch, int64_t Tq, int Tk, int causal, int64_t qoff,
+               float scale) {
     pdl_begin();
     using Tr = Traits<T>;
     constexpr int V = Tr::kVec;
@@ -190,8 +191,11 @@ softmax_fw_vec(T *out, const T *inp, const T *mask, int64_t rows,
         const int qi = (valid && causal) ? (int)(cp.q + qoff) : Tk;  // last visible key
         const T *mrow = (valid && mask) ? mask + cp.b * (int64_t)Tk : nullptr;
 
+        // SCALED: plain chunks keep x (their maximum mp is scaled once,
+        // below) and mixed chunks hold z = scale * x + mask; otherwise scale
+        // is 1 and every chunk holds z
         float2 v[CPT][H2];
-        float m = -INFINITY;
+        float m = -INFINITY, mp = -INFINITY;
 #pragma unroll
         for (int kk = 0; kk < CPT; ++kk) {
             const int c = kk * TPR + lane;
@@ -206,26 +210,39 @@ softmax_fw_vec(T *out, const T *inp, const T *mask, int64_t rows,
 #pragma unroll
                     for (int h = 0; h < H2; ++h) {
                         const int j = c * V + 2 * h;
-                        v[kk][h].x = j > qi ? -INFINITY : v[kk][h].x + mv[h].x;
-                        v[kk][h].y = j + 1 > qi ? -INFINITY : v[kk][h].y + mv[h].y;
+                        if constexpr (SCALED) {
+                            v[kk][h].x = j > qi ? -INFINITY : fmaf(v[kk][h].x, scale, mv[h].x);
+                            v[kk][h].y = j + 1 > qi ? -INFINITY : fmaf(v[kk][h].y, scale, mv[h].y);
+                        } else {
+                            v[kk][h].x = j > qi ? -INFINITY : v[kk][h].x + mv[h].x;
+                            v[kk][h].y = j + 1 > qi ? -INFINITY : v[kk][h].y + mv[h].y;
+                        }
                     }
-                }
 #pragma unroll
-                for (int h = 0; h < H2; ++h) m = fmax3(m, v[kk][h].x, v[kk][h].y);
+                    for (int h = 0; h < H2; ++h) m = fmax3(m, v[kk][h].x, v[kk][h].y);
+                } else {
+#pragma unroll
+                    for (int h = 0; h < H2; ++h) mp = fmax3(mp, v[kk][h].x, v[kk][h].y);
+                }
             }
         }
+        // scale > 0: the maximum of scale * x is scale * mp
+        m = fmaxf(m, SCALED ? mp * scale : mp);
         m = group_reduce<TPR, OpMax>(m, red);
-        // e = 2^(v*log2e - m*log2e); a row with no visible key sums to 0
+        // e = 2^(z*log2e - m*log2e), z*log2e taken as x*(scale*log2e) on plain
+        // chunks; a row with no visible key sums to 0
         const float mL = m == -INFINITY ? 0.f : m * kLog2e;
+        const float sl2 = SCALED ? scale * kLog2e : kLog2e;
         float2 sum2 = f2(0.f);
 #pragma unroll
         for (int kk = 0; kk < CPT; ++kk) {
             const int c = kk * TPR + lane;
             const uint32_t cls = (ccls >> (2 * kk)) & 3u;
             if (valid && c < nchunk && cls != kChunkSkip) {
+                const float2 mul = f2((!SCALED || cls == kChunkMixed) ? kLog2e : sl2);
 #pragma unroll
                 for (int h = 0; h < H2; ++h) {
-                    float2 t = fma2(v[kk][h], f2(kLog2e), f2(-mL));
+                    float2 t = fma2(v[kk][h], mul, f2(-mL));
                     t.x = fast_exp2(t.x);
                     t.y = fast_exp2(t.y);
                     v[kk][h] = t;
@@ -321,7 +338,8 @@ softmax_bw_vec(T *dinp, const T *dout, const T *y, int64_t rows, int Tk) {
 template <typename T, int TPR>
 __global__ void __launch_bounds__(TPR <= 32 ? 256 : TPR)
 softmax_fw_loop(T *out, const T *inp, const T *mask, int64_t rows,
-                int64_t rows_per_batch, int64_t Tq, int64_t Tk, int causal, int64_t qoff) {
+                int64_t rows_per_batch, int64_t Tq, int64_t Tk, int causal, int64_t qoff,
+                float scale) {
     pdl_begin();
     using Tr = Traits<T>;
     constexpr int BLOCK = TPR <= 32 ? 256 : TPR;
@@ -343,7 +361,7 @@ softmax_fw_loop(T *out, const T *inp, const T *mask, int64_t rows,
         for (int64_t j = lane; j < jend; j += TPR) {
             const float mv = mrow ? Tr::load1_cached(mrow + j) : 0.f;
             if (mv == -INFINITY) continue;
-            const float z = (Tr::load1(xrow + j) + mv) * kLog2e;
+            const float z = fmaf(Tr::load1(xrow + j), scale, mv) * kLog2e;
             if (z > m) {  // new running max: rescale what was summed so far
                 s = (m == -INFINITY ? 0.f : s * exp2f(m - z)) + 1.f;
                 m = z;
@@ -362,7 +380,7 @@ softmax_fw_loop(T *out, const T *inp, const T *mask, int64_t rows,
                 if (j < jend) {
                     const float mv = mrow ? Tr::load1_cached(mrow + j) : 0.f;
                     if (mv != -INFINITY)
-                        yv = exp2f((Tr::load1(xrow + j) + mv) * kLog2e - m) * inv;
+                        yv = exp2f(fmaf(Tr::load1(xrow + j), scale, mv) * kLog2e - m) * inv;
                 }
                 Tr::store1(orow + j, yv);
             }
@@ -409,7 +427,8 @@ softmax_bw_loop(T *dinp, const T *dout, const T *y, int64_t rows, int64_t Tk) {
 template <typename T, int TPR, int CPT>
 __global__ void __launch_bounds__(TPR <= 32 ? 256 : TPR)
 softmax_bw_masked_vec(T *dinp, const T *dout, const T *y, const T *mask, int64_t rows,
-                      int64_t rows_per_batch, int64_t Tq, int Tk, int causal, int64_t qoff) {
+                      int64_t rows_per_batch, int64_t Tq, int Tk, int causal, int64_t qoff,
+                      float scale) {
     pdl_begin();
     using Tr = Traits<T>;
     constexpr int V = Tr::kVec;
@@ -492,7 +511,8 @@ softmax_bw_masked_vec(T *dinp, const T *dout, const T *y, const T *mask, int64_t
                 unpack2<T>(gr[kk], gv);
 #pragma unroll
                 for (int h = 0; h < H2; ++h) {
-                    const float2 t = mul2(yv[h], add2(gv[h], f2(-s)));
+                    // scale * y * (g - s), with scale folded into the difference
+                    const float2 t = mul2(yv[h], fma2(gv[h], f2(scale), f2(-s * scale)));
                     dv[h].x = (vis[kk] >> (2 * h)) & 1u ? t.x : 0.f;
                     dv[h].y = (vis[kk] >> (2 * h + 1)) & 1u ? t.y : 0.f;
                 }
@@ -508,7 +528,7 @@ template <typename T, int TPR>
 __global__ void __launch_bounds__(TPR <= 32 ? 256 : TPR)
 softmax_bw_masked_loop(T *dinp, const T *dout, const T *y, const T *mask, int64_t rows,
                        int64_t rows_per_batch, int64_t Tq, int64_t Tk, int causal,
-                       int64_t qoff) {
+                       int64_t qoff, float scale) {
     pdl_begin();
     using Tr = Traits<T>;
     constexpr int BLOCK = TPR <= 32 ? 256 : TPR;
@@ -535,7 +555,7 @@ softmax_bw_masked_loop(T *dinp, const T *dout, const T *y, const T *mask, int64_
             for (int64_t j = lane; j < Tk; j += TPR) {
                 float d = 0.f;
                 if (j < jend && !(mrow && Tr::load1_cached(mrow + j) == -INFINITY))
-                    d = Tr::load1(y + off + j) * (Tr::load1(dout + off + j) - s);
+                    d = Tr::load1(y + off + j) * fmaf(Tr::load1(dout + off + j), scale, -s * scale);
                 Tr::store1(dinp + off + j, d);
             }
     }
