@@ -206,6 +206,24 @@ def test_encoder_big_layer_pass_bf16():
         compare(b.dbeta.cpu()[cols], rb, c.dtype, f"{c.name} dbeta")
 
 
+def test_overlapped_pass_matches_the_serial_pass():
+    """dgamma/dbeta on a side stream (the benchmark's schedule) gives exactly
+    the outputs of the one-stream pass, over several passes in a row."""
+    from transformer_reduce_gb300 import workloads as W
+    from transformer_reduce_gb300.layer_path import LayerReducePath
+    mk = lambda: LayerReducePath(W.GPT2_SMALL["softmax"],  # noqa: E731
+                                 [W.GPT2_SMALL["layernorm"], W.TINY["layernorm"]], device=DEV)
+    a, b = mk(), mk()
+    st = torch.cuda.current_stream()
+    side = torch.cuda.Stream()
+    for _ in range(3):
+        a.run(st)
+        b.run_overlapped(st, side)
+    torch.cuda.synchronize()
+    for x, y in zip(a._outputs(), b._outputs()):
+        assert torch.equal(x, y)
+
+
 def test_pipelined_passes_deliver_the_plain_pass_outputs():
     """The end-to-end schedule (two device buffer sets, copies on their own
     streams) brings back exactly what one plain pass computes."""

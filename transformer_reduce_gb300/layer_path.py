@@ -129,6 +129,37 @@ class LayerReducePath:
             e1.record(stream)
             timers.setdefault(name, []).append((e0, e1))
 
+    def run_overlapped(self, stream, side):
+        """One pass with the gamma/beta gradients on a second stream.
+
+        Nothing later in a layer's backward reads dgamma / dbeta (they are
+        parameter gradients), so each LayerNorm's dgamma/dbeta call runs on
+        `side` beside the rest of the backward on `stream`: it starts once
+        that LayerNorm's forward statistics exist and overlaps the input
+        gradient, the softmax backward and the other LayerNorm's calls.  The
+        pass ends with `stream` waiting for `side`, so the next pass (which
+        rewrites the statistics) starts after both.  Same calls and results
+        as run(); only the order between independent calls differs."""
+        st, sd = stream.cuda_stream, side.cuda_stream
+        ln1 = self.ln[0]
+        ln2 = self.ln[1] if len(self.ln) > 1 else None
+        self._ln_fw(ln1, st)
+        self._softmax_fw(st)
+        if ln2 is not None:
+            self._ln_fw(ln2, st)
+        fw_done = torch.cuda.Event()
+        fw_done.record(stream)
+        side.wait_event(fw_done)
+        if ln2 is not None:
+            self._ln_dgdb(ln2, sd)
+            self._ln_dinp(ln2, st)
+        self._softmax_bw(st)
+        self._ln_dgdb(ln1, sd)
+        self._ln_dinp(ln1, st)
+        side_done = torch.cuda.Event()
+        side_done.record(side)
+        stream.wait_event(side_done)
+
     # ---- accounting ----------------------------------------------------------
     def kernel_bytes(self) -> dict:
         """Algorithmic bytes of each call of one pass (name -> list of bytes)."""
@@ -197,7 +228,8 @@ class PipelinedPasses:
     """Passes fed from pinned host memory with the copies overlapped.
 
     Two device copies of the pass's buffers (``paths[0]`` and ``paths[1]``);
-    step k uses copy k % 2.  The host-to-device copies, the kernels and the
+    step k uses copy k % 2 (its kernels as ``run_overlapped`` schedules
+    them).  The host-to-device copies, the kernels and the
     device-to-host copies run on their own streams; each copy direction is
     split over ``lanes`` streams (tensors dealt out largest first), so that
     several copy engines work at once.  Events order step k's upload after
@@ -215,6 +247,7 @@ class PipelinedPasses:
         self.hin, self.hout = paths[0].host_buffers()
         self.s_up = [torch.cuda.Stream(self.dev) for _ in range(lanes)]
         self.s_run = torch.cuda.Stream(self.dev)
+        self.s_side = torch.cuda.Stream(self.dev)
         self.s_down = [torch.cuda.Stream(self.dev) for _ in range(lanes)]
         self.in_lane = self._deal([h.numel() * h.element_size() for h in self.hin], lanes)
         self.out_lane = self._deal([h.numel() * h.element_size() for h in self.hout], lanes)
@@ -261,7 +294,7 @@ class PipelinedPasses:
             if k >= 2:
                 for e in down[k - 2]:
                     self.s_run.wait_event(e)
-            p.run(self.s_run)
+            p.run_overlapped(self.s_run, self.s_side)
             comp.append(torch.cuda.Event())
             comp[k].record(self.s_run)
             for st in self.s_down:
