@@ -13,7 +13,9 @@ between passes, stays small while the tensors still exceed L2.
 --sweep times every kernel on every workload of ``workloads`` (softmax: the
 tiny, GPT-2-small, length-sweep and encoder cases; LayerNorm: the tiny,
 GPT-2-small, width-sweep and encoder cases).  Each launch is timed alone with
-CUDA events on its stream, after an L2 flush (a write of 2x the L2 size); one
+CUDA events on its stream, after an L2 flush (a read of 2x the L2 size: it
+evicts the kernel's inputs and leaves no dirty lines whose write-back would
+run during the timed launch); one
 JSON line per (kernel, workload) gives the median time and the algorithmic
 GB/s (``traffic``).  These are per-kernel context numbers; the benchmark
 proper is bench.py.
@@ -148,11 +150,14 @@ def prepare(kernel: str, case, dev):
 def time_kernel(call, launches: int, dev) -> list:
     """Per-launch device times (ms), each launch after an L2 flush."""
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    flush = torch.empty(2 * l2 // 4 + 1024, device=dev, dtype=torch.float32)
+    flush = torch.ones(2 * l2 // 4 + 1024, device=dev, dtype=torch.float32)
+    sink = torch.empty((), device=dev, dtype=torch.float32)
     stream = torch.cuda.current_stream(dev)
     out = []
     for _ in range(launches + 2):
-        flush.fill_(1.0)
+        # reads 2x L2 and writes 4 bytes; stream order puts it before e0, and
+        # the launch below is queued while it runs (no idle gap before e0)
+        torch.sum(flush, dim=0, out=sink)
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
         e0.record(stream)
