@@ -458,6 +458,63 @@ def test_outputs_stay_inside_their_buffers():
             assert torch.all(buf[:G] == -12345.0) and torch.all(buf[-G:] == -12345.0)
 
 
+def test_widened_outputs_stay_inside_their_buffers():
+    """Guard bands around the outputs and workspaces of the widened entry
+    points (masked and scaled softmax, fused LayerNorm backward, RMSNorm,
+    cross entropy) are left untouched."""
+    L = _L()
+    from transformer_reduce_gb300 import workloads as W
+    G = 4096
+    SENT = -12345.0
+
+    def guarded(numel, dtype):
+        buf = torch.full((numel + 2 * G,), SENT, device=DEV, dtype=dtype)
+        return buf, buf[G:G + numel]
+
+    bufs = []
+    for case, ln, vocab in [(_softmax_case(2, 3, 100, True, (50, 100), "bf16"), _ln_case(7, 100, "bf16"), 1001),
+                            (_softmax_case(2, 3, 512, False, (300, 512), "bf16"), _ln_case(309, 1024, "bf16"), 50257),
+                            (_softmax_case(1, 2, 64, True, None, "f32"), _ln_case(5, 4096, "f32"), 77)]:
+        dt = _dt(case.dtype)
+        inp = W.softmax_inputs(case, device=DEV)
+        n = inp["scores"].numel()
+        ybuf, y = guarded(n, dt)
+        L.softmax_fw(inp["scores"], inp["mask"], case.causal, out=y.view(case.shape), scale=0.25)
+        dbuf, d = guarded(n, dt)
+        L.softmax_bw_masked(inp["dout"], y.view(case.shape), inp["mask"], case.causal,
+                            dinp=d.view(case.shape), scale=0.25)
+        bufs += [ybuf, dbuf]
+        li = W.layernorm_inputs(ln, device=DEV)
+        R, N = ln.rows, ln.hidden
+        _, m, r = L.layernorm_fw(li["x"], li["gamma"], li["beta"], 1e-8)
+        n_ws = L.ls_layernorm_bw_workspace_size(R, N)
+        wsbuf, ws = guarded(max(n_ws, 16) // 4, torch.float32)
+        dxbuf, dx = guarded(R * N, dt)
+        gbuf, gg = guarded(N, torch.float32)
+        bbuf, bb = guarded(N, torch.float32)
+        L.layernorm_bw(li["dy"], li["x"], li["gamma"], m, r, workspace=ws, dx=dx.view(R, N),
+                       dgamma=gg, dbeta=bb)
+        rybuf, ry = guarded(R * N, dt)
+        rrbuf, rr = guarded(R, torch.float32)
+        L.rmsnorm_fw(li["x"], li["gamma"], 1e-6, y=ry.view(R, N), rstd=rr)
+        rdxbuf, rdx = guarded(R * N, dt)
+        L.rmsnorm_bw_dinp(li["dy"], li["x"], li["gamma"], rr, dx=rdx.view(R, N))
+        rgbuf, rg = guarded(N, torch.float32)
+        L.rmsnorm_bw_dgamma(li["dy"], li["x"], rr, dgamma=rg)
+        bufs += [wsbuf, dxbuf, gbuf, bbuf, rybuf, rrbuf, rdxbuf, rgbuf]
+        ce = W.CrossEntropyCase("guard", 1, 13, vocab, (10, 12), 3.0, case.dtype, 3)
+        ci = W.cross_entropy_inputs(ce, device=DEV)
+        lbuf, lo = guarded(13, torch.float32)
+        sbuf, ls = guarded(13, torch.float32)
+        L.cross_entropy_fw(ci["logits"], ci["target"], loss=lo, lse=ls)
+        zbuf, dz = guarded(13 * vocab, dt)
+        L.cross_entropy_bw(ci["logits"], ci["target"], ls, ci["dloss"], dlogits=dz.view(13, vocab))
+        bufs += [lbuf, sbuf, zbuf]
+    torch.cuda.synchronize()
+    for buf in bufs:
+        assert torch.all(buf[:G] == SENT) and torch.all(buf[-G:] == SENT)
+
+
 # ----------------------------------------------------------------------------
 # causal with Tq < Tk, and the masked backward
 # ----------------------------------------------------------------------------

@@ -322,7 +322,7 @@ cudaError_t launch_ln_dgdb(float *dgamma, float *dbeta, const T *dy, const T *x,
             if (e != cudaSuccess) return e;
         } else {
             dim3 grid((unsigned)ceil_div(N, 32), (unsigned)nchunks);
-            cudaError_t e = launch_pdl(ln_dgdb_partial<T, 1>, grid, dim3(kDgdbWarps * 32), 0, st,
+            cudaError_t e = launch_pdl(ln_dgdb_partial<T>, grid, dim3(kDgdbWarps * 32), 0, st,
                                        part, dy, x, mean, rstd, rows, N, rpc);
             if (e != cudaSuccess) return e;
         }

@@ -592,102 +592,62 @@ ln_dinp_loop(T *dx, const T *dy, const T *x, const T *gamma, const float *mean,
 }
 
 // ----------------------------------------------------------------------------
-// gamma / beta gradient, stage 1: partial column sums of one row chunk.
-// Block = 8 warps.  A warp spans one column tile (32 lanes x V columns: 16
-// bytes per lane, 512 contiguous bytes per row for 16-bit storage); warp w
-// takes rows w, w+8, ... of the chunk.  The 8 per-warp sums are then added in
-// warp order through shared memory and written to
+// gamma / beta gradient, stage 1, scalar path (any alignment or width):
+// partial column sums of one row chunk.  Block = 8 warps over a tile of 32
+// columns; warp w takes rows w, w+8, ... of the chunk, four rows in flight
+// per lane.  The 8 per-warp sums are added in warp order through shared
+// memory and written to
 //   part[(chunk * 2 + 0) * N + col] (dgamma),  part[(chunk * 2 + 1) * N + col] (dbeta).
-// V = 1 is the scalar path (any alignment).
+// mean == nullptr means mean 0 (RMSNorm).
 // ----------------------------------------------------------------------------
 constexpr int kDgdbWarps = 8;
 
-template <typename T, int V>
+template <typename T>
 __global__ void __launch_bounds__(kDgdbWarps * 32, 4)
 ln_dgdb_partial(float *part, const T *dy, const T *x, const float *mean,
                 const float *rstd, int64_t rows, int64_t N, int64_t rows_per_chunk) {
     pdl_begin();
     using Tr = Traits<T>;
-    constexpr int CT = 32 * V;  // columns per tile
+    constexpr int CT = 32;  // columns per tile
     __shared__ float sg[kDgdbWarps][CT];
     __shared__ float sb[kDgdbWarps][CT];
 
     const int lane = threadIdx.x & 31;
     const int w = threadIdx.x >> 5;
-    const int64_t col0 = (int64_t)blockIdx.x * CT + lane * V;
+    const int64_t col0 = (int64_t)blockIdx.x * CT + lane;
     const int64_t chunk = blockIdx.y;
     const int64_t r0 = chunk * rows_per_chunk;
     const int64_t r1 = min(rows, r0 + rows_per_chunk);
 
-    float ag[V], ab[V];
-#pragma unroll
-    for (int e = 0; e < V; ++e) ag[e] = ab[e] = 0.f;
-
+    float ag = 0.f, ab = 0.f;
     if (col0 < N) {
         int64_t r = r0 + w;
-        // Four rows in flight per warp per iteration.
         for (; r + 3 * kDgdbWarps < r1; r += 4 * kDgdbWarps) {
-            float mu[4], rs[4];
-            if constexpr (V == 1) {
-                float dv[4], xv[4];
+            float mu[4], rs[4], dv[4], xv[4];
 #pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const int64_t rr = r + u * kDgdbWarps;
-                    mu[u] = mean ? __ldg(mean + rr) : 0.f;
-                    rs[u] = __ldg(rstd + rr);
-                    dv[u] = Tr::load1(dy + rr * N + col0);
-                    xv[u] = Tr::load1(x + rr * N + col0);
-                }
+            for (int u = 0; u < 4; ++u) {
+                const int64_t rr = r + u * kDgdbWarps;
+                mu[u] = mean ? __ldg(mean + rr) : 0.f;
+                rs[u] = __ldg(rstd + rr);
+                dv[u] = Tr::load1(dy + rr * N + col0);
+                xv[u] = Tr::load1(x + rr * N + col0);
+            }
 #pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    ag[0] = fmaf(dv[u], (xv[u] - mu[u]) * rs[u], ag[0]);
-                    ab[0] += dv[u];
-                }
-            } else {
-                uint4 rdy[4], rx[4];  // raw 16-byte chunks: 4 rows in flight
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const int64_t rr = r + u * kDgdbWarps;
-                    mu[u] = mean ? __ldg(mean + rr) : 0.f;
-                    rs[u] = __ldg(rstd + rr);
-                    rdy[u] = ld_stream16(dy + rr * N + col0);
-                    rx[u] = ld_stream16(x + rr * N + col0);
-                }
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    float dv[V], xv[V];
-                    Tr::unpack(rdy[u], dv);
-                    Tr::unpack(rx[u], xv);
-#pragma unroll
-                    for (int e = 0; e < V; ++e) {
-                        ag[e] = fmaf(dv[e], (xv[e] - mu[u]) * rs[u], ag[e]);
-                        ab[e] += dv[e];
-                    }
-                }
+            for (int u = 0; u < 4; ++u) {
+                ag = fmaf(dv[u], (xv[u] - mu[u]) * rs[u], ag);
+                ab += dv[u];
             }
         }
         for (; r < r1; r += kDgdbWarps) {
-            float dv[V], xv[V];
             const float mu = mean ? __ldg(mean + r) : 0.f, rs = __ldg(rstd + r);
-            if constexpr (V == 1) {
-                dv[0] = Tr::load1(dy + r * N + col0);
-                xv[0] = Tr::load1(x + r * N + col0);
-            } else {
-                Tr::unpack(ld_stream16(dy + r * N + col0), dv);
-                Tr::unpack(ld_stream16(x + r * N + col0), xv);
-            }
-#pragma unroll
-            for (int e = 0; e < V; ++e) {
-                ag[e] = fmaf(dv[e], (xv[e] - mu) * rs, ag[e]);
-                ab[e] += dv[e];
-            }
+            const float dv = Tr::load1(dy + r * N + col0);
+            const float xv = Tr::load1(x + r * N + col0);
+            ag = fmaf(dv, (xv - mu) * rs, ag);
+            ab += dv;
         }
     }
-#pragma unroll
-    for (int e = 0; e < V; ++e) {
-        sg[w][lane * V + e] = ag[e];
-        sb[w][lane * V + e] = ab[e];
-    }
+    sg[w][lane] = ag;
+    sb[w][lane] = ab;
     __syncthreads();
     for (int cc = threadIdx.x; cc < CT; cc += kDgdbWarps * 32) {
         const int64_t col = (int64_t)blockIdx.x * CT + cc;
@@ -705,11 +665,12 @@ ln_dgdb_partial(float *part, const T *dy, const T *x, const float *mean,
 }
 
 // ----------------------------------------------------------------------------
-// gamma / beta gradient, stage 1, vectorised: the same partial sums as
-// ln_dgdb_partial (the same tiles, warp-to-row assignment, fp32 arithmetic and
-// warp-order combine), with each warp streaming its rows through a private
-// ring of kDgdbStages cp.async stages of kDgdbRows rows each (512 contiguous
-// bytes of dy and of x per row, plus the rows' mean and rstd), so that
+// gamma / beta gradient, stage 1, vectorised: the partial sums of
+// ln_dgdb_partial over tiles of 32 lanes x 16 bytes (256 columns of 16-bit
+// storage), with the same warp-to-row assignment, fp32 arithmetic and
+// warp-order combine; each warp streams its rows through a private ring of
+// kDgdbStages cp.async stages of kDgdbRows rows each (512 contiguous bytes of
+// dy and of x per row, plus the rows' mean and rstd), so that
 // (kDgdbStages - 1) * kDgdbRows rows per warp are in flight and the per-stage
 // bookkeeping is shared by kDgdbRows rows.  The ring is reused for the
 // warp-order combine at the end.  mean == nullptr means mean 0 (RMSNorm).
