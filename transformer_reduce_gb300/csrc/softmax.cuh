@@ -419,14 +419,130 @@ softmax_bw_loop(T *dinp, const T *dout, const T *y, int64_t rows, int64_t Tk) {
 }
 
 // ----------------------------------------------------------------------------
-// Masked backward: dinp_j = y_j (dout_j - sum over visible k of y_k dout_k)
-// on visible keys, 0 elsewhere.  Chunks whose keys are all invisible (mask
-// -inf, or causal future) are neither read nor summed; they are written as
-// zeros.  Same row mapping as softmax_bw_vec, rows of a group contiguous.
+// Masked backward: dinp_j = scale * y_j (dout_j - sum over visible k of
+// y_k dout_k) on visible keys, 0 elsewhere.  Chunks whose keys are all
+// invisible (mask -inf, or causal future) are neither read nor summed; they
+// are written as zeros.  This form serves rows of up to three chunks per
+// thread: same row mapping as softmax_bw_vec (rows strided over the grid);
+// each row finds its batch entry and query by division and classifies its
+// mask chunks afresh (the mask row stays in L1), so nothing is carried from
+// row to row and the kernel stays near the plain backward's register budget
+// and occupancy.  Longer rows take softmax_bw_masked_runs below.
 // ----------------------------------------------------------------------------
 template <typename T, int TPR, int CPT>
 __global__ void __launch_bounds__(TPR <= 32 ? 256 : TPR)
 softmax_bw_masked_vec(T *dinp, const T *dout, const T *y, const T *mask, int64_t rows,
+                      int64_t rows_per_batch, int64_t Tq, int Tk, int causal, int64_t qoff,
+                      float scale) {
+    pdl_begin();
+    using Tr = Traits<T>;
+    constexpr int V = Tr::kVec;
+    constexpr int H2 = V / 2;
+    constexpr int BLOCK = TPR <= 32 ? 256 : TPR;
+    constexpr int G = BLOCK / TPR;
+    __shared__ float red[TPR > 32 ? 64 : 1];
+
+    const int lane = threadIdx.x % TPR;
+    const int grp = threadIdx.x / TPR;
+    const int nchunk = Tk / V;
+    const bool narrow = rows <= INT32_MAX && rows_per_batch <= INT32_MAX && Tq <= INT32_MAX;
+
+    for (int64_t base = (int64_t)blockIdx.x * G; base < rows;
+         base += (int64_t)gridDim.x * G) {
+        const int64_t row = base + grp;
+        const bool valid = row < rows;
+        const int64_t off = row * (int64_t)Tk;
+        // batch entry and last visible key of this row
+        int64_t b = 0, q = 0;
+        if (valid && (mask || causal)) {
+            if (narrow) {
+                const uint32_t r32 = (uint32_t)row;
+                b = r32 / (uint32_t)rows_per_batch;
+                q = causal ? r32 % (uint32_t)Tq : 0;
+            } else {
+                b = row / rows_per_batch;
+                q = causal ? row % Tq : 0;
+            }
+        }
+        const int64_t qi = causal ? q + qoff : (int64_t)Tk;
+        const T *mrow = (valid && mask) ? mask + b * (int64_t)Tk : nullptr;
+
+        uint4 yr[CPT], gr[CPT];
+        uint32_t vis[CPT];  // visible elements of each chunk (bit e)
+#pragma unroll
+        for (int kk = 0; kk < CPT; ++kk) {
+            const int c = kk * TPR + lane;
+            yr[kk] = gr[kk] = make_uint4(0u, 0u, 0u, 0u);
+            vis[kk] = 0u;
+            if (!valid || c >= nchunk) continue;
+            uint32_t bits = (1u << V) - 1u;
+            if (mrow) {
+                float mv[V];
+                Tr::unpack(ld_cached16(mrow + c * V), mv);
+                bits = 0u;
+#pragma unroll
+                for (int e = 0; e < V; ++e) bits |= (mv[e] != -INFINITY ? 1u : 0u) << e;
+            }
+            if (causal) {
+                const int64_t j0 = (int64_t)c * V;
+#pragma unroll
+                for (int e = 0; e < V; ++e)
+                    if (j0 + e > qi) bits &= ~(1u << e);
+            }
+            vis[kk] = bits;
+            if (bits) {
+                yr[kk] = ld_stream16(y + off + c * V);
+                gr[kk] = ld_stream16(dout + off + c * V);
+            }
+        }
+        float2 s2 = f2(0.f);
+#pragma unroll
+        for (int kk = 0; kk < CPT; ++kk) {
+            float2 yv[H2], gv[H2];
+            unpack2<T>(yr[kk], yv);
+            unpack2<T>(gr[kk], gv);
+            if (vis[kk] == (1u << V) - 1u) {
+#pragma unroll
+                for (int h = 0; h < H2; ++h) s2 = fma2(yv[h], gv[h], s2);
+            } else {
+#pragma unroll
+                for (int h = 0; h < H2; ++h) {
+                    const float2 p = mul2(yv[h], gv[h]);
+                    s2.x += (vis[kk] >> (2 * h)) & 1u ? p.x : 0.f;
+                    s2.y += (vis[kk] >> (2 * h + 1)) & 1u ? p.y : 0.f;
+                }
+            }
+        }
+        const float s = group_reduce<TPR, OpSum>(s2.x + s2.y, red);
+#pragma unroll
+        for (int kk = 0; kk < CPT; ++kk) {
+            const int c = kk * TPR + lane;
+            if (valid && c < nchunk) {
+                float2 yv[H2], gv[H2], dv[H2];
+                unpack2<T>(yr[kk], yv);
+                unpack2<T>(gr[kk], gv);
+#pragma unroll
+                for (int h = 0; h < H2; ++h) {
+                    // scale * y * (g - s), with scale folded into the difference
+                    const float2 t = mul2(yv[h], fma2(gv[h], f2(scale), f2(-s * scale)));
+                    dv[h].x = (vis[kk] >> (2 * h)) & 1u ? t.x : 0.f;
+                    dv[h].y = (vis[kk] >> (2 * h + 1)) & 1u ? t.y : 0.f;
+                }
+                st_stream16(dinp + off + c * V, pack2<T>(dv));
+            }
+        }
+    }
+}
+
+// ----------------------------------------------------------------------------
+// Masked backward for rows of four or more chunks per thread: each row group
+// takes a contiguous run of rows, so the mask chunk classes are cached per
+// batch entry (RowClasses) and the row position advances without division
+// (RowPos); per-element visibility is kept for every chunk.
+// ----------------------------------------------------------------------------
+template <typename T, int TPR, int CPT>
+__global__ void __launch_bounds__(TPR <= 32 ? 256 : TPR)
+softmax_bw_masked_runs(T *dinp, const T *dout, const T *y, const T *mask, int64_t rows,
                       int64_t rows_per_batch, int64_t Tq, int Tk, int causal, int64_t qoff,
                       float scale) {
     pdl_begin();
