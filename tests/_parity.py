@@ -29,6 +29,11 @@ def _key16(t: torch.Tensor) -> torch.Tensor:
     return torch.where((bits & 0x8000) != 0, -(bits & 0x7FFF), bits)
 
 
+# Error statistics of every comparison of the session, written out as JSON
+# lines by conftest.py when LS_PARITY_REPORT names a file.
+REPORT = []
+
+
 def compare(gpu: torch.Tensor, ref: np.ndarray, cfg_dtype: str, what: str) -> dict:
     """Assert the tolerance rule element by element; return error statistics."""
     gpu = gpu.detach().cpu()
@@ -42,7 +47,10 @@ def compare(gpu: torch.Tensor, ref: np.ndarray, cfg_dtype: str, what: str) -> di
     if gpu.dtype == torch.bfloat16:
         r16 = torch.from_numpy(ref).to(torch.bfloat16)
         d = (_key16(gpu) - _key16(r16)).abs().numpy()
-        max_ulp = int(d.max()) if d.size else 0
+        # reported over the values the absolute tolerance does not cover
+        # (near zero a bf16 step is tiny and the step count meaningless)
+        big = np.abs(ref) >= tol
+        max_ulp = int(d[big].max()) if np.any(big) else 0
         ok |= d <= 1
     assert np.all(np.isfinite(g)), f"{what}: non-finite output"
     n_bad = int((~ok).sum())
@@ -50,8 +58,15 @@ def compare(gpu: torch.Tensor, ref: np.ndarray, cfg_dtype: str, what: str) -> di
         idx = np.argwhere(~ok)[:5]
         detail = [(tuple(int(v) for v in i), float(g[tuple(i)]), float(ref[tuple(i)])) for i in idx]
         raise AssertionError(f"{what}: {n_bad}/{ok.size} elements out of tolerance, e.g. {detail}")
-    return {"what": what, "n": int(ok.size), "strict_frac": float(strict.mean()) if ok.size else 1.0,
-            "max_abs": float(err.max()) if err.size else 0.0, "max_bf16_steps": max_ulp}
+    rel = err / np.maximum(np.abs(ref), np.finfo(np.float64).tiny)
+    stats = {"what": what, "cfg_dtype": cfg_dtype, "out_dtype": str(gpu.dtype).replace("torch.", ""),
+             "n": int(ok.size), "strict_frac": float(strict.mean()) if ok.size else 1.0,
+             "max_abs": float(err.max()) if err.size else 0.0,
+             "max_rel_where_ref_ge_1e-3": float(rel[np.abs(ref) >= 1e-3].max())
+             if np.any(np.abs(ref) >= 1e-3) else 0.0,
+             "max_bf16_steps": max_ulp, "tol": tol}
+    REPORT.append(stats)
+    return stats
 
 
 def sample_rows(nrows: int, boundaries=(), k: int = 192, seed: int = 0) -> np.ndarray:

@@ -21,3 +21,18 @@ def ref():
     import oracle
     oracle.build()
     return oracle
+
+
+def pytest_sessionfinish(session, exitstatus):
+    """With LS_PARITY_REPORT set, write the error statistics of every GPU-vs-
+    oracle comparison of the session as JSON lines to that file."""
+    path = os.environ.get("LS_PARITY_REPORT")
+    if not path:
+        return
+    mod = sys.modules.get("_parity")
+    if mod is None or not mod.REPORT:
+        return
+    import json
+    with open(path, "w", encoding="utf-8") as f:
+        for rec in mod.REPORT:
+            f.write(json.dumps(rec) + "\n")
