@@ -15,7 +15,7 @@
 // logits it reads, the pairs are merged across the row group, and
 // lse = ln 2 * (m + log2 s).  A row of vocabulary size V starts at an
 // arbitrary element offset (V need not be a multiple of the 16-byte vector),
-// so each row is split into a scalar head up to the first 16-byte boundary, a
+// so each row is split into a scalar head up to the first 128-byte boundary, a
 // body of 16-byte vectors and a scalar tail.  Ignored rows (target < 0) are
 // not read.
 #pragma once
@@ -36,7 +36,10 @@ template <int TPR>
 constexpr int ce_block() { return TPR < 128 ? 256 : TPR; }
 
 // Head / body / tail of a row that starts at p: `head` scalars up to the
-// first 16-byte boundary, then `nbody` whole vectors.  vec == false puts the
+// first 128-byte boundary, then `nbody` whole 16-byte vectors.  Starting the
+// body on a cache line makes every warp's 512-byte access four whole lines
+// (from a mere 16-byte boundary it straddles a fifth line, and the partial
+// sectors at both ends are read and written twice).  vec == false puts the
 // whole row in the head (scalar path).
 template <typename T>
 __device__ __forceinline__ void ce_split(const T *p, int64_t V, bool vec, int64_t &head,
@@ -48,7 +51,7 @@ __device__ __forceinline__ void ce_split(const T *p, int64_t V, bool vec, int64_
         return;
     }
     const uintptr_t a = reinterpret_cast<uintptr_t>(p);
-    int64_t h = (int64_t)(((16u - (unsigned)(a & 15u)) & 15u) / sizeof(T));
+    int64_t h = (int64_t)(((128u - (unsigned)(a & 127u)) & 127u) / sizeof(T));
     head = h < V ? h : V;
     nbody = (V - head) / VV;
 }
