@@ -266,8 +266,8 @@ size_t ls_layernorm_bw_workspace_size(int64_t rows, int64_t hidden);
  *                  ls_layernorm_bw_workspace_size(rows, hidden) bytes,
  *                  16-byte aligned, contents ignored; may be NULL when that
  *                  size is 0.  Calls that overlap on the GPU must not share it.
- * Errors as for ls_layernorm_bw_dgamma_dbeta.  Rows wider than 1024 16-byte
- * vectors (hidden > 8192 for 16-bit storage, > 4096 for fp32), or pointers
+ * Errors as for ls_layernorm_bw_dgamma_dbeta.  Rows wider than 2048 16-byte
+ * vectors (hidden > 16384 for 16-bit storage, > 8192 for fp32), or pointers
  * or widths that are not 16-byte multiples, run the two separate kernels
  * instead, with the same results as calling them.
  */

@@ -766,7 +766,8 @@ def test_ln_bw_fused_small_configs_and_encoder():
 
 @pytest.mark.parametrize("dtype", ["f32", "f16", "bf16"])
 @pytest.mark.parametrize("rows,N", [(1, 64), (7, 1024), (303, 256), (304, 512), (305, 768),
-                                    (1000, 2048), (21, 7), (21, 770), (21, 20000)])
+                                    (1000, 2048), (333, 8192), (9, 16384), (21, 7), (21, 770),
+                                    (21, 20000)])
 def test_ln_bw_fused_ragged_chunks_and_widths(dtype, rows, N):
     # row counts around the 304-chunk cut (one row per chunk, a ragged last
     # chunk) and widths that take the scalar two-kernel path

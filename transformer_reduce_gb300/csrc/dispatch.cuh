@@ -344,7 +344,7 @@ cudaError_t launch_ln_dgdb(float *dgamma, float *dbeta, const T *dy, const T *x,
 // (one chunk per thread measured slower: more threads and barriers per row).
 #define LSR_FUSED_BW_BUCKETS(X)                                                 \
     X(1, 1) X(1, 2) X(2, 2) X(4, 2) X(8, 2) X(16, 2) X(32, 2) X(64, 2) X(128, 2) \
-    X(256, 2) X(512, 2)
+    X(128, 3) X(128, 4) X(256, 2) X(256, 3) X(256, 4) X(512, 3) X(512, 4)
 constexpr int kFusedMaxCpt = 2;
 
 
@@ -354,7 +354,13 @@ cudaError_t launch_ln_bw_fused(T *dx, float *dgamma, float *dbeta, const T *dy, 
                                int64_t rows, int64_t N, float *part, bool vec, cudaStream_t st) {
     constexpr int V = Traits<T>::kVec;
     int tpr = 0, cpt = 0;
-    if (rows > 0 && vec && pick_bucket_dense(N / V, kFusedMaxCpt, kLnMaxTpr, &tpr, &cpt)) {
+    // rows of more than 256 vectors take up to 4 chunks per thread (the row's
+    // g and xhat are then unpacked again for the epilogue instead of held):
+    // fewer, fuller threads per row, two 256-thread blocks per SM
+    const int64_t nvec = N / V;
+    const bool picked = nvec <= 256 ? pick_bucket_dense(nvec, kFusedMaxCpt, kLnMaxTpr, &tpr, &cpt)
+                                    : pick_bucket_dense(nvec, kLnMaxCpt, kLnMaxTpr, &tpr, &cpt);
+    if (rows > 0 && vec && picked) {
         int64_t nparts = 0;
         cudaError_t e = cudaErrorInvalidValue;
 #define X(TPR_, CPT_)                                                                       \
@@ -375,7 +381,7 @@ cudaError_t launch_ln_bw_fused(T *dx, float *dgamma, float *dbeta, const T *dy, 
                           dim3(kFinalCols * kFinalLanes), 0, st, dgamma, dbeta,
                           (const float *)part, nparts, N);
     }
-    // rows that take the scalar path, or wider than 2 * 512 vectors: the two
+    // rows that take the scalar path, or wider than 4 * 512 vectors: the two
     // kernels one after the other
     cudaError_t e = launch_ln_dinp<T>(dx, dy, x, gamma, mean, rstd, rows, N, vec, st);
     if (e != cudaSuccess) return e;

@@ -416,25 +416,43 @@ ln_bw_fused_vec(T *dx, float *part, const T *dy, const T *x, const T *gamma, con
         const bool valid = row < rend;
         const float mu = valid ? stat[(s_cur * 2 + 0) * BLOCK + tid] : 0.f;
         const float rs = valid ? stat[(s_cur * 2 + 1) * BLOCK + tid] : 0.f;
-        float2 g[CPT][H2], xh[CPT][H2];
+        // Up to two chunks per thread the row's g and xhat stay in registers
+        // for the epilogue; wider buckets (whose column accumulators already
+        // take 64 registers) unpack them again from the stage instead.
+        constexpr bool kKeep = CPT <= 2;
+        float2 g[kKeep ? CPT : 1][H2], xh[kKeep ? CPT : 1][H2];
         float2 s1 = f2(0.f), s2 = f2(0.f);
+        auto load_row = [&](int kk, float2 (&gg)[H2], float2 (&xx)[H2]) {
+            float2 gv[H2];
+            unpack2<T>(stage[((s_cur * 2 + 0) * CPT + kk) * BLOCK + tid], gg);
+            unpack2<T>(stage[((s_cur * 2 + 1) * CPT + kk) * BLOCK + tid], xx);
+            unpack2<T>(gr[kk], gv);
+#pragma unroll
+            for (int h = 0; h < H2; ++h) {
+                xx[h] = mul2(add2(xx[h], f2(-mu)), f2(rs));
+                gg[h] = mul2(gg[h], gv[h]);
+            }
+        };
 #pragma unroll
         for (int kk = 0; kk < CPT; ++kk) {
             const int c = kk * TPR + lane;
             if (valid && c < nchunk) {
-                float2 gv[H2];
-                unpack2<T>(stage[((s_cur * 2 + 0) * CPT + kk) * BLOCK + tid], g[kk]);
-                unpack2<T>(stage[((s_cur * 2 + 1) * CPT + kk) * BLOCK + tid], xh[kk]);
-                unpack2<T>(gr[kk], gv);
+                float2 dv[H2], gg[H2], xx[H2];
+                unpack2<T>(stage[((s_cur * 2 + 0) * CPT + kk) * BLOCK + tid], dv);
+                load_row(kk, gg, xx);
 #pragma unroll
                 for (int h = 0; h < H2; ++h) {
-                    // g[kk][h] still holds dy here: the column sums take it first
-                    ab[kk][h] = add2(ab[kk][h], g[kk][h]);
-                    xh[kk][h] = mul2(add2(xh[kk][h], f2(-mu)), f2(rs));
-                    ag[kk][h] = fma2(g[kk][h], xh[kk][h], ag[kk][h]);
-                    g[kk][h] = mul2(g[kk][h], gv[h]);
-                    s1 = add2(s1, g[kk][h]);
-                    s2 = fma2(g[kk][h], xh[kk][h], s2);
+                    ab[kk][h] = add2(ab[kk][h], dv[h]);
+                    ag[kk][h] = fma2(dv[h], xx[h], ag[kk][h]);
+                    s1 = add2(s1, gg[h]);
+                    s2 = fma2(gg[h], xx[h], s2);
+                }
+                if constexpr (kKeep) {
+#pragma unroll
+                    for (int h = 0; h < H2; ++h) {
+                        g[kk][h] = gg[h];
+                        xh[kk][h] = xx[h];
+                    }
                 }
             }
         }
@@ -446,10 +464,19 @@ ln_bw_fused_vec(T *dx, float *part, const T *dy, const T *x, const T *gamma, con
         for (int kk = 0; kk < CPT; ++kk) {
             const int c = kk * TPR + lane;
             if (valid && c < nchunk) {
-                float2 ov[H2];
+                float2 gg[H2], xx[H2], ov[H2];
+                if constexpr (kKeep) {
+#pragma unroll
+                    for (int h = 0; h < H2; ++h) {
+                        gg[h] = g[kk][h];
+                        xx[h] = xh[kk][h];
+                    }
+                } else {
+                    load_row(kk, gg, xx);
+                }
 #pragma unroll
                 for (int h = 0; h < H2; ++h)
-                    ov[h] = mul2(f2(rs), fma2(xh[kk][h], nb, add2(g[kk][h], na)));
+                    ov[h] = mul2(f2(rs), fma2(xx[h], nb, add2(gg[h], na)));
                 st_stream16(dx + off + c * V, pack2<T>(ov));
             }
         }
