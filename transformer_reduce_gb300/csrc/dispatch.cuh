@@ -354,12 +354,14 @@ cudaError_t launch_ln_bw_fused(T *dx, float *dgamma, float *dbeta, const T *dy, 
                                int64_t rows, int64_t N, float *part, bool vec, cudaStream_t st) {
     constexpr int V = Traits<T>::kVec;
     int tpr = 0, cpt = 0;
-    // rows of more than 256 vectors take up to 4 chunks per thread (the row's
-    // g and xhat are then unpacked again for the epilogue instead of held):
-    // fewer, fuller threads per row, two 256-thread blocks per SM
+    // Chunks per thread: two (the row's g and xhat held for the epilogue) up
+    // to 256 vectors; four above (g and xhat unpacked again from the staged
+    // row), where 256 threads with four chunks beat 512 with two (8192
+    // features on GB300: 179 -> 143 us).
     const int64_t nvec = N / V;
-    const bool picked = nvec <= 256 ? pick_bucket_dense(nvec, kFusedMaxCpt, kLnMaxTpr, &tpr, &cpt)
-                                    : pick_bucket_dense(nvec, kLnMaxCpt, kLnMaxTpr, &tpr, &cpt);
+    const bool four = nvec > 256;
+    const bool picked = pick_bucket_dense(nvec, four ? kLnMaxCpt : kFusedMaxCpt, kLnMaxTpr, &tpr,
+                                          &cpt);
     if (rows > 0 && vec && picked) {
         int64_t nparts = 0;
         cudaError_t e = cudaErrorInvalidValue;
