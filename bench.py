@@ -275,6 +275,41 @@ def host_cores() -> int:
 # our arm
 # ---------------------------------------------------------------------------
 
+def host_link(dev, nbytes: int = 256 << 20, reps: int = 3) -> dict:
+    """Copy-engine bandwidth between pinned host memory and this GPU: each
+    direction alone, then both at once on two streams (GB/s each way).  The
+    end-to-end pass cannot move its host bytes faster than this."""
+    h_in = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+    h_out = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+    d_in = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    d_out = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    s_up, s_down = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+
+    def timed(up: bool, down: bool) -> float:
+        torch.cuda.synchronize(dev)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        s_up.wait_event(e0)
+        s_down.wait_event(e0)
+        for _ in range(reps):
+            if up:
+                with torch.cuda.stream(s_up):
+                    d_in.copy_(h_in, non_blocking=True)
+            if down:
+                with torch.cuda.stream(s_down):
+                    h_out.copy_(d_out, non_blocking=True)
+        for s in (s_up, s_down):
+            torch.cuda.current_stream(dev).wait_stream(s)
+        e1.record()
+        torch.cuda.synchronize(dev)
+        return reps * nbytes / (e0.elapsed_time(e1) / 1e3) / 1e9
+
+    timed(True, True)  # warm-up
+    return {"h2d_gbs": round(timed(True, False), 1), "d2h_gbs": round(timed(False, True), 1),
+            "both_gbs_each_way": round(timed(True, True), 1)}
+
+
 def run_ours(args):
     world, rank, local = dist_env()
     if not torch.cuda.is_available():
@@ -362,6 +397,11 @@ def run_ours(args):
     barrier(world)
     e2e_s = max_over_ranks(e0.elapsed_time(e1) / 1e3, world)
     e2e_value = sum_over_ranks(step_bytes * e2e_steps, world) / e2e_s / 1e9
+    link = host_link(dev)
+    # lower bound of an end-to-end step: its larger copy direction at the
+    # both-directions rate (the copies of a step overlap each other)
+    link["floor_ms_per_step"] = round(
+        max(path.h2d_bytes(), path.d2h_bytes()) / (link["both_gbs_each_way"] * 1e9) * 1e3, 4)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -395,7 +435,8 @@ def run_ours(args):
             "cpu_baseline": cpu,
             "e2e": {"value": round(e2e_value, 1), "unit": "GB/s",
                     "h2d_bytes_per_step": path.h2d_bytes(), "d2h_bytes_per_step": path.d2h_bytes(),
-                    "steps": e2e_steps, "ms_per_step": round(e2e_s / e2e_steps * 1e3, 4)},
+                    "steps": e2e_steps, "ms_per_step": round(e2e_s / e2e_steps * 1e3, 4),
+                    "host_link": link},
             "clocks": clk,
             "gpu_launches": launches_per_step * args.steps,
         }
