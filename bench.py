@@ -430,6 +430,10 @@ def run_ours(args):
             "pct_of_peak": round(100 * value / world / peak, 2),
             "rows_per_s": {k: round(world * v * args.steps / job_s) for k, v in rows.items()},
             "bytes_per_step": step_bytes,
+            "dense_equivalent": {
+                "bytes_per_step": path.dense_step_bytes(),
+                "gbs": round(world * path.dense_step_bytes() * args.steps / job_s / 1e9, 1),
+                "note": "as if the softmax forward read masked keys too"},
             "kernels": kernels,
             "roofline": roofline,
             "cpu_baseline": cpu,

@@ -180,6 +180,16 @@ class LayerReducePath:
     def step_bytes(self) -> int:
         return sum(sum(v) for v in self.kernel_bytes().values())
 
+    def dense_step_bytes(self) -> int:
+        """Bytes of one pass if the softmax forward read every key (no
+        masked-key skipping): the dense-equivalent count."""
+        s = self.sm
+        skipped = (traffic.softmax_fw_bytes(s.B, s.H, s.T, [s.T] * s.B, False, s.dtype,
+                                            self.mask is not None)
+                   - traffic.softmax_fw_bytes(s.B, s.H, s.T, self.lengths, s.causal, s.dtype,
+                                              self.mask is not None))
+        return self.step_bytes() + skipped
+
     def rows(self) -> dict:
         return {"softmax_rows": 2 * self.sm.rows,  # forward and backward
                 "layernorm_rows": sum(3 * b.case.rows for b in self.ln)}
