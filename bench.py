@@ -14,8 +14,18 @@ With N > 1 (launched by torch.distributed.run) every rank runs its own
 replica of the pass on its own GPU (the rows are independent; there is no
 data-path collective); the job time is the maximum over ranks.
 
---impl reference times the CPU oracle (fp64 C, one host core) on a bounded
-row sample of the same workload; it is a deliberately slow baseline.
+Besides the headline the line carries, each measured over at least
+--kernel-seconds of device time whatever --steps is: the per-kernel times of
+the pass (``kernels``); every kernel alone with a cold L2 on the large
+configurations -- softmax [8,16,T,T] bf16 for T in {768, 1024, 2048} and
+LayerNorm [16384, N] bf16 for N in {4096, 8192} -- and on the encoder shapes
+(``large_configs``, ``encoder_cold``); the widened kernels (``next_rows``);
+the same layer with the fused LayerNorm backward and the masked softmax
+backward (``fused_pass``); and the end-to-end pass fed from pinned host
+memory (``e2e``).
+
+--impl reference times the CPU oracle (fp64 C, on all host cores) on a
+bounded row sample of the same workload; it is a deliberately slow baseline.
 """
 from __future__ import annotations
 
@@ -310,6 +320,68 @@ def host_link(dev, nbytes: int = 256 << 20, reps: int = 3) -> dict:
             "both_gbs_each_way": round(timed(True, True), 1)}
 
 
+# Kernels launched per call of each pass entry (ln_dgdb and the fused
+# LayerNorm backward are a partial-sum kernel plus the fixed-order final sum).
+KERNELS_PER_CALL = {"ln_dgdb": 2, "ln_bw": 2}
+
+# Cold-L2 single-kernel measurements: (kernel, workload) pairs.
+LARGE_CONFIGS = ([(k, f"softmax_T{T}") for T in (768, 1024, 2048)
+                  for k in ("softmax_fw", "softmax_bw")]
+                 + [(k, f"layernorm_N{N}") for N in (4096, 8192)
+                    for k in ("ln_fw", "ln_dinp", "ln_dgdb")])
+ENCODER_COLD = [("softmax_fw", "encoder_big"), ("softmax_bw", "encoder_big"),
+                ("ln_fw", "encoder_big"), ("ln_dinp", "encoder_big"),
+                ("ln_dgdb", "encoder_big")]
+NEXT_ROWS = [("softmax_bw_masked", "encoder_big"), ("softmax_bw_masked", "softmax_T1024"),
+             ("ln_bw", "encoder_big"), ("ln_bw", "layernorm_N4096"),
+             ("ln_bw", "layernorm_N8192"), ("rms_fw", "layernorm_N8192"),
+             ("rms_dinp", "layernorm_N8192"), ("ce_fw", "ce_gpt2"), ("ce_bw", "ce_gpt2")]
+
+
+def cold_table(jobs, dev, peak, min_seconds):
+    """Each (kernel, workload) launched alone after an L2 read-flush, timed
+    with CUDA events on its stream over at least `min_seconds` of device time;
+    only that kernel's buffers are allocated."""
+    from transformer_reduce_gb300 import profile_kernel as pk
+    from transformer_reduce_gb300 import workloads
+    out = {}
+    for kernel, wname in jobs:
+        if kernel.startswith("ce"):
+            case = pk.CE_CASES[wname]
+        elif wname == "encoder_big":
+            case = workloads.ENCODER_BIG["softmax"] if kernel.startswith("softmax") \
+                else workloads.ENCODER_BIG["layernorm"][0]
+        else:
+            case = (pk.SOFTMAX_CASES if kernel.startswith("softmax") else pk.LN_CASES)[wname]
+        call, nbytes, keep = pk.prepare(kernel, case, dev)
+        ms = pk.time_kernel(call, 20, dev, min_seconds=min_seconds)
+        mean_ms = sum(ms) / len(ms)
+        gbs = nbytes / (mean_ms / 1e3) / 1e9
+        out[f"{kernel}@{case.name}"] = {
+            "kernel": kernel, "workload": case.name, "dtype": case.dtype,
+            "launches": len(ms), "mean_us": round(mean_ms * 1e3, 2),
+            "median_us": round(statistics.median(ms) * 1e3, 2),
+            "bytes": nbytes, "gbs": round(gbs, 1), "frac_of_peak": round(gbs / peak, 4)}
+        del keep, call
+        torch.cuda.empty_cache()
+    return out
+
+
+def kernel_stats(timers, kbytes, peak):
+    kernels = {}
+    for name, pairs in timers.items():
+        ms = [a.elapsed_time(b) for a, b in pairs]
+        per_launch = kbytes[name]
+        calls_per_step = len(per_launch)
+        avg_ms = sum(ms) / len(ms)
+        bytes_per_call = sum(per_launch) / calls_per_step
+        gbs = bytes_per_call / (avg_ms / 1e3) / 1e9
+        kernels[name] = {"calls_per_step": calls_per_step, "calls_timed": len(ms),
+                         "avg_ms": round(avg_ms, 5), "bytes_per_call": int(bytes_per_call),
+                         "gbs": round(gbs, 1), "frac_of_peak": round(gbs / peak, 4)}
+    return kernels
+
+
 def run_ours(args):
     world, rank, local = dist_env()
     if not torch.cuda.is_available():
@@ -326,8 +398,9 @@ def run_ours(args):
     side = torch.cuda.Stream(dev)  # the gamma/beta gradients beside the backward
     step_bytes = path.step_bytes()
     kbytes = path.kernel_bytes()
-    launches_per_step = sum(2 if n == "ln_dgdb" else 1 for n, _ in path.sequence())
+    launches_per_step = sum(KERNELS_PER_CALL.get(n, 1) for n, _ in path.sequence())
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    min_s = args.kernel_seconds
 
     clocks = ClockSampler(local)
     for _ in range(args.warmup):
@@ -349,11 +422,12 @@ def run_ours(args):
     torch.cuda.synchronize(dev)
     clk = clocks.stop()
     elapsed_s = t0.elapsed_time(t1) / 1e3
+    pass_s = elapsed_s / args.steps
     # timed region 2: the same calls one after the other on one stream with an
     # event pair around every call, for each kernel's own launch duration
-    # (the roofline's denominator)
+    # (the roofline's denominator); at least min_s of passes
     timers = {}
-    kernel_steps = max(1, min(args.steps, 1000))
+    kernel_steps = max(args.steps, int(min_s / pass_s) + 1)
     for _ in range(kernel_steps):
         path.run(stream, timers=timers)
     torch.cuda.synchronize(dev)
@@ -363,17 +437,7 @@ def run_ours(args):
     value = total_bytes / job_s / 1e9
 
     peak, peak_src = hbm_peak()
-    kernels = {}
-    for name, pairs in timers.items():
-        ms = [a.elapsed_time(b) for a, b in pairs]
-        per_launch = kbytes[name]
-        calls_per_step = len(per_launch)
-        avg_ms = sum(ms) / len(ms)
-        bytes_per_call = sum(per_launch) / calls_per_step
-        gbs = bytes_per_call / (avg_ms / 1e3) / 1e9
-        kernels[name] = {"calls_per_step": calls_per_step, "avg_ms": round(avg_ms, 5),
-                         "bytes_per_call": int(bytes_per_call), "gbs": round(gbs, 1),
-                         "frac_of_peak": round(gbs / peak, 4)}
+    kernels = kernel_stats(timers, kbytes, peak)
     dom = kernels[DOMINANT]
     traffic = ncu_traffic()
     roofline = {"bound": "hbm", "kernel": "softmax_bw_vec<bf16,32,2>", "achieved": dom["gbs"],
@@ -381,15 +445,51 @@ def run_ours(args):
                 "frac": round(dom["gbs"] / peak, 4), "traffic": traffic,
                 "algorithmic_bytes": dom["bytes_per_call"]}
 
+    # the same layer with the fused LayerNorm backward and the masked softmax
+    # backward, one stream, at least min_s of passes
+    fused_bytes = path.fused_step_bytes()
+    for _ in range(args.warmup):
+        path.run_fused(stream)
+    torch.cuda.synchronize(dev)
+    f0 = torch.cuda.Event(enable_timing=True)
+    f1 = torch.cuda.Event(enable_timing=True)
+    fused_steps = max(args.steps, int(min_s / pass_s) + 1)
+    f0.record(stream)
+    for _ in range(fused_steps):
+        path.run_fused(stream)
+    f1.record(stream)
+    torch.cuda.synchronize(dev)
+    fused_s = max_over_ranks(f0.elapsed_time(f1) / 1e3, world)
+    ftimers = {}
+    for _ in range(kernel_steps):
+        path.run_fused(stream, timers=ftimers)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    fused_pass = {
+        "calls": [n for n, _ in path.fused_sequence()],
+        "steps": fused_steps, "ms_per_step": round(fused_s / fused_steps * 1e3, 5),
+        "bytes_per_step": fused_bytes,
+        "gbs": round(sum_over_ranks(fused_bytes * fused_steps, world) / fused_s / 1e9, 1),
+        "rows_per_s": {k: round(world * v * fused_steps / fused_s)
+                       for k, v in path.rows().items()},
+        "kernels": kernel_stats(ftimers, path.fused_kernel_bytes(), peak),
+        "note": "one stream; the same outputs as the headline pass up to the fused "
+                "kernels' own summation order"}
+
     # end to end: every input copied from pinned host memory to the device,
     # the pass, every output copied back, each step; copies overlapped with
     # the kernels of neighbouring steps on their own streams (two device
     # buffer sets)
-    e2e_steps = max(3, min(args.steps // 20, 30))
+    link = host_link(dev)
+    # lower bound of an end-to-end step: its larger copy direction at the
+    # both-directions rate (the copies of a step overlap each other)
+    link["floor_ms_per_step"] = round(
+        max(path.h2d_bytes(), path.d2h_bytes()) / (link["both_gbs_each_way"] * 1e9) * 1e3, 4)
+    e2e_steps = max(30, int(min_s / (link["floor_ms_per_step"] / 1e3)) + 1)
     twin = LayerReducePath(workloads.ENCODER_BIG["softmax"], workloads.ENCODER_BIG["layernorm"],
                            device=dev)
     pipe = PipelinedPasses([path, twin])
-    pipe.run(2)  # warm-up: both buffer sets, copy engines
+    pipe.run(4)  # warm-up: both buffer sets, copy engines
     torch.cuda.synchronize(dev)
     barrier(world)
     e0, e1 = pipe.run(e2e_steps)
@@ -397,11 +497,15 @@ def run_ours(args):
     barrier(world)
     e2e_s = max_over_ranks(e0.elapsed_time(e1) / 1e3, world)
     e2e_value = sum_over_ranks(step_bytes * e2e_steps, world) / e2e_s / 1e9
-    link = host_link(dev)
-    # lower bound of an end-to-end step: its larger copy direction at the
-    # both-directions rate (the copies of a step overlap each other)
-    link["floor_ms_per_step"] = round(
-        max(path.h2d_bytes(), path.d2h_bytes()) / (link["both_gbs_each_way"] * 1e9) * 1e3, 4)
+    del twin, pipe
+    torch.cuda.empty_cache()
+
+    # every kernel alone with a cold L2: the large configurations, the
+    # encoder shapes and the widened kernels (only that kernel's buffers are
+    # allocated; the pass's buffers stay)
+    large = cold_table(LARGE_CONFIGS, dev, peak, min_s) if not args.no_cold else None
+    enc_cold = cold_table(ENCODER_COLD, dev, peak, min_s) if not args.no_cold else None
+    nxt = cold_table(NEXT_ROWS, dev, peak, min_s) if not args.no_cold else None
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -416,15 +520,19 @@ def run_ours(args):
                "single_core_value": round(sample.bytes / per_pass_1 / 1e9, 4)}
 
     rows = path.rows()
+    ln_mb = path.ln[0].x.numel() * path.ln[0].x.element_size() / 1e6
     if rank == 0:
         line = {
             "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(job_s / args.steps * 1e3, 5), "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "compute": "f32",
+            "data": "synthetic",
             "config": {"workload": WORKLOAD, "storage": "bf16", "parallelism": "replicas",
-                       "schedule": "dgamma/dbeta calls on a second stream beside the rest "
-                                   "of the backward; per-kernel times from a one-stream pass",
+                       "schedule": "dgamma/dbeta on a second stream: LN2's once the forward "
+                                   "statistics exist, LN1's once the softmax backward is done "
+                                   "(when its dy would exist); per-kernel times from a "
+                                   "one-stream pass",
                        "l2": f"inputs larger than L2 (pass moves {step_bytes / 1e9:.2f} GB; "
                              f"L2 {l2 / 1e6:.0f} MB); no flush"},
             "pct_of_peak": round(100 * value / world / peak, 2),
@@ -435,12 +543,23 @@ def run_ours(args):
                 "gbs": round(world * path.dense_step_bytes() * args.steps / job_s / 1e9, 1),
                 "note": "as if the softmax forward read masked keys too"},
             "kernels": kernels,
+            "kernels_note": (f"in-pass, one stream, {kernel_steps} passes; each LayerNorm tensor "
+                             f"({ln_mb:.1f} MB) fits in L2, so ln_dinp and ln_dgdb may find x "
+                             "and dy that the call before them read still in L2; encoder_cold "
+                             "has every kernel alone after an L2 flush"),
             "roofline": roofline,
             "cpu_baseline": cpu,
             "e2e": {"value": round(e2e_value, 1), "unit": "GB/s",
                     "h2d_bytes_per_step": path.h2d_bytes(), "d2h_bytes_per_step": path.d2h_bytes(),
                     "steps": e2e_steps, "ms_per_step": round(e2e_s / e2e_steps * 1e3, 4),
                     "host_link": link},
+            "fused_pass": fused_pass,
+            "large_configs": large,
+            "encoder_cold": enc_cold,
+            "next_rows": nxt,
+            "cold_note": (f"each kernel alone after a read of 2x L2, CUDA events on its stream, "
+                          f"at least {min_s} s of device time per entry; frac_of_peak uses the "
+                          "mean launch time"),
             "clocks": clk,
             "gpu_launches": launches_per_step * args.steps,
         }
@@ -502,6 +621,11 @@ def main(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="minimum host time spent timing the CPU oracle sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--kernel-seconds", type=float, default=0.3,
+                    help="minimum device time of each per-kernel, fused-pass, end-to-end and "
+                         "cold-L2 measurement")
+    ap.add_argument("--no-cold", action="store_true",
+                    help="skip the cold-L2 single-kernel tables")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

@@ -305,9 +305,13 @@ ls_status ls_layernorm_bw(void *dx, float *dgamma, float *dbeta, const void *dy,
  *   (ls_layernorm_bw_dgamma_dbeta_workspace_size(rows, hidden) larger than
  *   that) are refused with LS_ERR_UNSUPPORTED before anything is launched.
  *
- * The first call on each device looks up the array's device address
- * (cudaGetSymbolAddress) with that device current and caches it; make that
- * first call before any stream capture.  All calls on a device share the one
+ * Every call looks up the array's device address (cudaGetSymbolAddress) with
+ * the caller's device current; once the library's module is loaded on that
+ * device the lookup is a host-side query that allocates nothing, and a fresh
+ * lookup stays valid after cudaDeviceReset.  The first call on a device may
+ * be the one that loads the module, which places the array in device memory
+ * and can synchronise: make one call during set-up, before any stream
+ * capture, if that must not happen later.  All calls on a device share the one
  * array: calls that may overlap on the GPU (different streams without
  * ordering between them) race on it and must not be issued that way.  The
  * array keeps the last call's partial sums; each call overwrites every

@@ -224,6 +224,32 @@ def test_overlapped_pass_matches_the_serial_pass():
         assert torch.equal(x, y)
 
 
+def test_fused_pass_matches_the_serial_pass():
+    """The layer with the fused LayerNorm backward and the masked softmax
+    backward (the benchmark's fused_pass) gives the outputs of the plain pass
+    within the tolerance rule; only summation orders differ."""
+    from transformer_reduce_gb300 import workloads as W
+    from transformer_reduce_gb300.layer_path import LayerReducePath
+    mk = lambda: LayerReducePath(W.ENCODER_BIG["softmax"],  # noqa: E731
+                                 W.ENCODER_BIG["layernorm"], device=DEV)
+    a = mk()
+    a.run()
+    torch.cuda.synchronize()
+    want = [t.clone() for t in a._outputs()]
+    for t in a._outputs():
+        t.fill_(float("nan"))
+    a.run_fused()
+    a.run_fused()
+    torch.cuda.synchronize()
+    names = ["probs", "dscores"] + [f"ln{i} {n}" for i in (1, 2)
+                                     for n in ("y", "mean", "rstd", "dx", "dgamma", "dbeta")]
+    rows = sample_rows(a.sm.rows, k=256, seed=3)
+    for name, got, ref in zip(names, a._outputs(), want):
+        if got.dim() == 4:
+            got, ref = take_rows(got, rows), take_rows(ref, rows)
+        compare(got, ref.double().cpu().numpy(), "bf16", f"fused pass {name}")
+
+
 def test_pipelined_passes_deliver_the_plain_pass_outputs():
     """The end-to-end schedule (two device buffer sets, copies on their own
     streams) brings back exactly what one plain pass computes."""

@@ -8,8 +8,9 @@ It keeps its partial sums in a fixed device array inside the library.
 
 This test calls it through the C ABI twice in a row, on two different
 problems, and checks each result against the workspace entry point
-ls_layernorm_bw_dgamma_dbeta with the tolerance rule of the parity tests
-(the second call must not see the first call's leftovers in the shared
+ls_layernorm_bw_dgamma_dbeta: within the tolerance rule of the parity tests,
+and bit for bit, since both run the same kernels in the same fixed summation
+order (the second call must not see the first call's leftovers in the shared
 array).  It also checks that a problem too large for the array is refused.
 The file name makes pytest collect it last.
 """
@@ -81,6 +82,8 @@ def test_no_alloc_matches_workspace_entry_point_on_two_calls_in_a_row(abi):
         torch.cuda.synchronize()
         compare(got_g, want_g.double().cpu().numpy(), name, f"no-alloc dgamma {rows}x{hidden}")
         compare(got_b, want_b.double().cpu().numpy(), name, f"no-alloc dbeta {rows}x{hidden}")
+        assert torch.equal(got_g, want_g), f"dgamma {rows}x{hidden} differs bitwise"
+        assert torch.equal(got_b, want_b), f"dbeta {rows}x{hidden} differs bitwise"
 
 
 def test_no_alloc_refuses_problems_beyond_its_array(abi):

@@ -13,13 +13,16 @@
 // The array is a file-scope __device__ variable: every GPU that loads the
 // library holds LS_DGDB_NOALLOC_SCRATCH_BYTES of it until the process exits.
 // Its name in host code is only a host-side stand-in, so the host never passes
-// it to a kernel; the device address is looked up once per device with
-// cudaGetSymbolAddress (the first call on a device does this) and cached.
+// it to a kernel.  Every call looks the device address up afresh with
+// cudaGetSymbolAddress, with the caller's device current: once the library's
+// module is loaded on a device that lookup is a host-side query that
+// allocates nothing, and a fresh lookup stays right after cudaDeviceReset,
+// which reloads the module and may move the array.  The first call on a device
+// may be the one that loads the module (placing the array in device memory);
+// callers that must not see that make one call during set-up.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
-
-#include <mutex>
 
 #include "launch.h"
 #include "ls_reduce.h"
@@ -31,22 +34,12 @@ constexpr size_t kScratchFloats = LS_DGDB_NOALLOC_SCRATCH_BYTES / sizeof(float);
 // The partial sums of every call live here (shared by all calls on a device).
 static __device__ __align__(256) float g_dgdb_scratch[kScratchFloats];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_mu;
-float *g_scratch_ptr[kMaxDevices] = {};
-
-// Device address of g_dgdb_scratch on the current device, looked up on first
-// use; nullptr if the runtime cannot provide it.
+// Device address of g_dgdb_scratch on the current device; nullptr if the
+// runtime cannot provide it.
 float *scratch_on_current_device() {
-    int dev = -1;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
-    std::lock_guard<std::mutex> lock(g_mu);
-    if (!g_scratch_ptr[dev]) {
-        void *p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_dgdb_scratch) != cudaSuccess || !p) return nullptr;
-        g_scratch_ptr[dev] = static_cast<float *>(p);
-    }
-    return g_scratch_ptr[dev];
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_dgdb_scratch) != cudaSuccess || !p) return nullptr;
+    return static_cast<float *>(p);
 }
 
 size_t elem_bytes(ls_dtype dt) {

@@ -41,6 +41,7 @@ class _LnBuffers:
     dgamma: torch.Tensor
     dbeta: torch.Tensor
     ws: torch.Tensor
+    ws_fused: torch.Tensor
 
 
 class LayerReducePath:
@@ -56,13 +57,15 @@ class LayerReducePath:
         for case in ln_cases:
             li = workloads.layernorm_inputs(case, device=self.device)
             n = _lib.ls_layernorm_bw_dgamma_dbeta_workspace_size(case.rows, case.hidden)
+            nf = _lib.ls_layernorm_bw_workspace_size(case.rows, case.hidden)
             f32 = dict(device=self.device, dtype=torch.float32)
             self.ln.append(_LnBuffers(
                 case=case, x=li["x"], gamma=li["gamma"], beta=li["beta"], dy=li["dy"],
                 y=torch.empty_like(li["x"]), mean=torch.empty(case.rows, **f32),
                 rstd=torch.empty(case.rows, **f32), dx=torch.empty_like(li["x"]),
                 dgamma=torch.empty(case.hidden, **f32), dbeta=torch.empty(case.hidden, **f32),
-                ws=torch.empty(max(n, 16) // 4, **f32)))
+                ws=torch.empty(max(n, 16) // 4, **f32),
+                ws_fused=torch.empty(max(nf, 16) // 4, **f32)))
         self._host = None
 
     # ---- the hot path ------------------------------------------------------
@@ -84,6 +87,21 @@ class LayerReducePath:
             b.dgamma.data_ptr(), b.dbeta.data_ptr(), b.dy.data_ptr(), b.x.data_ptr(),
             b.mean.data_ptr(), b.rstd.data_ptr(), c.rows, c.hidden, b.ws.data_ptr(),
             b.ws.numel() * 4, _DT[c.dtype], st), "ls_layernorm_bw_dgamma_dbeta")
+
+    def _ln_bw_fused(self, b: _LnBuffers, st):
+        c = b.case
+        _ok(_lib.ls_layernorm_bw(
+            b.dx.data_ptr(), b.dgamma.data_ptr(), b.dbeta.data_ptr(), b.dy.data_ptr(),
+            b.x.data_ptr(), b.gamma.data_ptr(), b.mean.data_ptr(), b.rstd.data_ptr(), c.rows,
+            c.hidden, b.ws_fused.data_ptr(), b.ws_fused.numel() * 4, _DT[c.dtype], st),
+            "ls_layernorm_bw")
+
+    def _softmax_bw_masked(self, st):
+        s = self.sm
+        _ok(_lib.ls_softmax_bw_masked(
+            self.dscores.data_ptr(), self.dprobs.data_ptr(), self.probs.data_ptr(),
+            0 if self.mask is None else self.mask.data_ptr(), s.B, s.H, s.T, s.T, s.causal,
+            _DT[s.dtype], st), "ls_softmax_bw_masked")
 
     def _softmax_fw(self, st):
         s = self.sm
@@ -112,13 +130,37 @@ class LayerReducePath:
                 ("ln_dgdb", lambda st: self._ln_dgdb(ln1, st))]
         return seq
 
+    def fused_sequence(self):
+        """The same layer with the fused LayerNorm backward (dx, dgamma and
+        dbeta from one read of dy and x) and the softmax backward that takes
+        the mask and reads only visible keys; (name, call) in stream order."""
+        ln1 = self.ln[0]
+        ln2 = self.ln[1] if len(self.ln) > 1 else None
+        seq = [("ln_fw", lambda st: self._ln_fw(ln1, st)),
+               ("softmax_fw", self._softmax_fw)]
+        if ln2 is not None:
+            seq += [("ln_fw", lambda st: self._ln_fw(ln2, st)),
+                    ("ln_bw", lambda st: self._ln_bw_fused(ln2, st))]
+        seq += [("softmax_bw_masked", self._softmax_bw_masked),
+                ("ln_bw", lambda st: self._ln_bw_fused(ln1, st))]
+        return seq
+
+    def run_fused(self, stream=None, timers=None):
+        """Enqueue one pass of fused_sequence() on one stream (timers as in
+        run()).  Same outputs as run(), up to the rounding of the fused
+        kernels' own summation order."""
+        self._enqueue(self.fused_sequence(), stream, timers)
+
     def run(self, stream=None, timers=None):
         """Enqueue one pass on `stream` (default: torch's current stream).
         timers: optional dict name -> list; a (start, end) CUDA event pair
         recorded on the same stream is appended around each call."""
+        self._enqueue(self.sequence(), stream, timers)
+
+    def _enqueue(self, seq, stream, timers):
         stream = stream or torch.cuda.current_stream(self.device)
         st = stream.cuda_stream
-        for name, call in self.sequence():
+        for name, call in seq:
             if timers is None:
                 call(st)
                 continue
@@ -134,12 +176,21 @@ class LayerReducePath:
 
         Nothing later in a layer's backward reads dgamma / dbeta (they are
         parameter gradients), so each LayerNorm's dgamma/dbeta call runs on
-        `side` beside the rest of the backward on `stream`: it starts once
-        that LayerNorm's forward statistics exist and overlaps the input
-        gradient, the softmax backward and the other LayerNorm's calls.  The
-        pass ends with `stream` waiting for `side`, so the next pass (which
-        rewrites the statistics) starts after both.  Same calls and results
-        as run(); only the order between independent calls differs."""
+        `side` beside the rest of the backward on `stream`, but no earlier
+        than a real layer could issue it:
+
+        * LN2's dy (the gradient arriving from the block above) exists when
+          the backward starts, so LN2's dgamma/dbeta starts once the forward
+          statistics exist and overlaps LN2's input gradient and the softmax
+          backward;
+        * LN1's dy is the attention block's input gradient, which exists only
+          after the softmax backward, so LN1's dgamma/dbeta waits for an event
+          recorded after the softmax backward and overlaps only LN1's own
+          input gradient.
+
+        The pass ends with `stream` waiting for `side`, so the next pass
+        (which rewrites the statistics) starts after both.  Same calls and
+        results as run(); only the order between independent calls differs."""
         st, sd = stream.cuda_stream, side.cuda_stream
         ln1 = self.ln[0]
         ln2 = self.ln[1] if len(self.ln) > 1 else None
@@ -147,13 +198,15 @@ class LayerReducePath:
         self._softmax_fw(st)
         if ln2 is not None:
             self._ln_fw(ln2, st)
-        fw_done = torch.cuda.Event()
-        fw_done.record(stream)
-        side.wait_event(fw_done)
-        if ln2 is not None:
+            fw_done = torch.cuda.Event()
+            fw_done.record(stream)
+            side.wait_event(fw_done)
             self._ln_dgdb(ln2, sd)
             self._ln_dinp(ln2, st)
         self._softmax_bw(st)
+        dy1_ready = torch.cuda.Event()
+        dy1_ready.record(stream)
+        side.wait_event(dy1_ready)
         self._ln_dgdb(ln1, sd)
         self._ln_dinp(ln1, st)
         side_done = torch.cuda.Event()
@@ -179,6 +232,21 @@ class LayerReducePath:
 
     def step_bytes(self) -> int:
         return sum(sum(v) for v in self.kernel_bytes().values())
+
+    def fused_kernel_bytes(self) -> dict:
+        """Algorithmic bytes of each call of one fused_sequence() pass."""
+        s = self.sm
+        kb = self.kernel_bytes()
+        out = {"ln_fw": kb["ln_fw"], "softmax_fw": kb["softmax_fw"], "ln_bw": [],
+               "softmax_bw_masked": [traffic.softmax_bw_masked_bytes(
+                   s.B, s.H, s.T, self.lengths, s.causal, s.dtype, self.mask is not None)]}
+        for b in self.ln:
+            c = b.case
+            out["ln_bw"].append(traffic.layernorm_bw_fused_bytes(c.rows, c.hidden, c.dtype))
+        return out
+
+    def fused_step_bytes(self) -> int:
+        return sum(sum(v) for v in self.fused_kernel_bytes().values())
 
     def dense_step_bytes(self) -> int:
         """Bytes of one pass if the softmax forward read every key (no

@@ -147,25 +147,42 @@ def prepare(kernel: str, case, dev):
         traffic.layernorm_dgdb_bytes(c.rows, c.hidden, c.dtype), keep
 
 
-def time_kernel(call, launches: int, dev) -> list:
-    """Per-launch device times (ms), each launch after an L2 flush."""
+def time_kernel(call, launches: int, dev, min_seconds: float = 0.0, warmup: int = 3,
+                max_launches: int = 100_000) -> list:
+    """Per-launch device times (ms), each launch timed alone after an L2 flush.
+
+    At least `launches` launches are timed, and more until their device time
+    adds up to `min_seconds` (capped at `max_launches`), after `warmup`
+    untimed launches.  The flush reads a buffer of twice the L2 size and
+    writes 4 bytes: it evicts the kernel's inputs and leaves no dirty lines
+    whose write-back would run during the timed launch.  Stream order puts it
+    before the start event and the launch is queued while it runs, so there
+    is no idle gap inside the timed interval."""
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     flush = torch.ones(2 * l2 // 4 + 1024, device=dev, dtype=torch.float32)
     sink = torch.empty((), device=dev, dtype=torch.float32)
     stream = torch.cuda.current_stream(dev)
-    out = []
-    for _ in range(launches + 2):
-        # reads 2x L2 and writes 4 bytes; stream order puts it before e0, and
-        # the launch below is queued while it runs (no idle gap before e0)
-        torch.sum(flush, dim=0, out=sink)
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        _ok(call(), "kernel")
-        e1.record(stream)
+
+    def batch(n):
+        ev = []
+        for _ in range(n):
+            torch.sum(flush, dim=0, out=sink)
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            _ok(call(), "kernel")
+            e1.record(stream)
+            ev.append((e0, e1))
         torch.cuda.synchronize(dev)
-        out.append(e0.elapsed_time(e1))
-    return out[2:]
+        return [a.elapsed_time(b) for a, b in ev]
+
+    batch(max(warmup, 1))
+    out = batch(max(launches, 1))
+    while sum(out) < min_seconds * 1e3 and len(out) < max_launches:
+        est = max(sum(out) / len(out), 1e-3)
+        need = int((min_seconds * 1e3 - sum(out)) / est) + 1
+        out += batch(min(max(need, 1), max_launches - len(out), 2000))
+    return out
 
 
 def main(argv=None):
