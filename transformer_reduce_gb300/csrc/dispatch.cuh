@@ -160,7 +160,8 @@ cudaError_t launch_softmax_fw(T *out, const T *inp, const T *mask, int64_t rows,
                               int causal, int64_t qoff, float scale, bool vec, cudaStream_t st) {
     constexpr int V = Traits<T>::kVec;
     int tpr = 0, cpt = 0;
-    if (vec && pick_bucket_dense(Tk / V, kSoftmaxFwMaxCpt, kSoftmaxFwMaxTpr, &tpr, &cpt)) {
+    if (vec && rows <= INT32_MAX &&
+        pick_bucket_dense(Tk / V, kSoftmaxFwMaxCpt, kSoftmaxFwMaxTpr, &tpr, &cpt)) {
 #define X(TPR_, CPT_)                                                                   \
     if (tpr == TPR_ && cpt == CPT_) {                                                   \
         if (scale == 1.0f)                                                              \
@@ -212,18 +213,13 @@ cudaError_t launch_softmax_bw_masked(T *dinp, const T *dout, const T *y, const T
                                      cudaStream_t st) {
     constexpr int V = Traits<T>::kVec;
     int tpr = 0, cpt = 0;
-    if (vec && pick_bucket(Tk / V, kSoftmaxBwMaxCpt, kSoftmaxBwMaxTpr, &tpr, &cpt)) {
+    if (vec && rows <= INT32_MAX &&
+        pick_bucket(Tk / V, kSoftmaxBwMaxCpt, kSoftmaxBwMaxTpr, &tpr, &cpt)) {
 #define X(TPR_, CPT_)                                                                   \
-    if (tpr == TPR_ && cpt == CPT_) {                                                   \
-        if constexpr (CPT_ <= 3)                                                        \
-            return launch_persistent<softmax_bw_masked_vec<T, TPR_, CPT_>>(             \
-                block_threads<TPR_>(), 0, ceil_div(rows, rows_per_block<TPR_>()), st, dinp, \
-                dout, y, mask, rows, rows_per_batch, Tq, (int)Tk, causal, qoff, scale);     \
-        else                                                                            \
-            return launch_persistent<softmax_bw_masked_runs<T, TPR_, CPT_>>(            \
-                block_threads<TPR_>(), 0, ceil_div(rows, rows_per_block<TPR_>()), st, dinp, \
-                dout, y, mask, rows, rows_per_batch, Tq, (int)Tk, causal, qoff, scale);     \
-    }
+    if (tpr == TPR_ && cpt == CPT_)                                                     \
+        return launch_persistent<softmax_bw_masked_vec<T, TPR_, CPT_>>(                 \
+            block_threads<TPR_>(), 0, ceil_div(rows, rows_per_block<TPR_>()), st, dinp,     \
+            dout, y, mask, rows, rows_per_batch, Tq, (int)Tk, causal, qoff, scale);
         LSR_SOFTMAX_BW_BUCKETS(X)
 #undef X
     }

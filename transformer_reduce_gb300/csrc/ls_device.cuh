@@ -387,4 +387,13 @@ __device__ __forceinline__ float fast_exp2(float x) {
     return y;
 }
 
+// 1/x with the hardware approximation (PTX rcp.approx.ftz.f32: at most one
+// unit in the last place off the correctly rounded result).  Used for the
+// softmax normaliser, a sum of at least 1 (the maximum's own term).
+__device__ __forceinline__ float fast_rcp(float x) {
+    float y;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 }  // namespace lsr

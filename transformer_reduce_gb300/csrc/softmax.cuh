@@ -17,7 +17,8 @@
 //    threads touch consecutive 16-byte chunks (fully coalesced 128-bit
 //    accesses).
 //  * Keys that are masked (-inf in the additive mask) or in the causal future
-//    are never read: a whole 16-byte chunk of them costs no HBM traffic.
+//    are never read when the mask is a window of visible keys (a padding
+//    mask): a whole 16-byte chunk of them costs no HBM traffic.
 //  * The grid is persistent: blocks loop over row groups, so the launch is
 //    sized from the SM count and occupancy, not the problem size.
 //  * Rows that do not fit the register buckets, or whose rows are not
@@ -31,99 +32,69 @@ namespace lsr {
 // ----------------------------------------------------------------------------
 // Register-resident forward: one row per TPR threads, CPT chunks per thread.
 //
-// Each row group owns a contiguous range of rows (rows of one batch entry
-// share the mask row) and keeps the next row's chunks in flight while it
-// reduces the current one.  Per 16-byte chunk the mask is classified once per
-// batch entry: all 0 (add nothing), all -inf (the chunk is neither read nor
-// exponentiated; it is written as zeros) or mixed (added element by element).
-// Causal rows test keys against the query only in the chunk that holds the
-// diagonal; chunks wholly in the future are skipped like masked ones.
+// A padding mask (additive, 0 on the keys a batch entry may attend to, -inf
+// on the others) almost always makes every row's visible keys one window
+// [lo, hi) of the row.  Each block therefore first classifies the mask rows
+// of the batch entries its rows belong to: a row whose elements are all 0 or
+// -inf and whose non-(-inf) keys are contiguous is the window [lo, hi); any
+// other row (finite non-zero biases, -inf holes inside the window) is
+// "general".  Per row, causal masking only lowers hi to the last visible key
+// + 1.  A chunk of V keys is then visible, fully visible or invisible by two
+// integer compares; invisible chunks are neither read nor exponentiated and
+// are written as zeros, and only the (at most two) chunks straddling lo or hi
+// need per-element work.  Rows of a general batch entry add the mask element
+// by element (and mask future keys one by one when causal); that path is
+// exact, just not the fast one.
+//
+// Each row group owns a contiguous range of rows and keeps the next S-1
+// rows' visible chunks in flight (cp.async into shared memory; each thread
+// reads back only its own slots) while it reduces the current one.
 // ----------------------------------------------------------------------------
-enum : uint32_t { kChunkPlain = 0u, kChunkSkip = 1u, kChunkMixed = 2u };
+constexpr int kWinMax = 64;        // batch entries a block classifies at most
+constexpr int kWinGeneral = -1;    // lo of a mask row that is not a window
 
-// Mask class of a 16-byte chunk of T (2 bits).
-template <typename T>
-__device__ __forceinline__ uint32_t mask_chunk_class(const uint4 &m) {
+// Window [lo, hi) of the mask row of one batch entry, found by one warp
+// (every lane returns it); lo = kWinGeneral for a row that is not a window.
+// A row with no visible key is the empty window [0, 0).  ADDS: the forward,
+// which adds the mask, needs every element to be 0 or -inf; the masked
+// backward only needs the keys that are not -inf to be contiguous.
+template <typename T, bool ADDS>
+__device__ __forceinline__ int2 mask_row_window(const T *mrow, int Tk) {
     using Tr = Traits<T>;
     constexpr int V = Tr::kVec;
-    float mv[V];
-    Tr::unpack(m, mv);
-    bool all_zero = true, all_ninf = true;
+    const int lane = threadIdx.x & 31;
+    const int nchunk = Tk / V;
+    int first = Tk, last = -1, count = 0, other = 0;
+    for (int c = lane; c < nchunk; c += 32) {
+        float mv[V];
+        Tr::unpack(ld_cached16(mrow + c * V), mv);
 #pragma unroll
-    for (int e = 0; e < V; ++e) {
-        all_zero &= (mv[e] == 0.f);
-        all_ninf &= (mv[e] == -INFINITY);
+        for (int e = 0; e < V; ++e) {
+            const bool ninf = mv[e] == -INFINITY;
+            if (ADDS) other |= !(ninf || mv[e] == 0.f);
+            if (!ninf) {
+                first = min(first, c * V + e);
+                last = max(last, c * V + e);
+                ++count;
+            }
+        }
     }
-    return all_ninf ? kChunkSkip : (all_zero ? kChunkPlain : kChunkMixed);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        first = min(first, __shfl_xor_sync(0xffffffffu, first, o));
+        last = max(last, __shfl_xor_sync(0xffffffffu, last, o));
+        count += __shfl_xor_sync(0xffffffffu, count, o);
+        other |= __shfl_xor_sync(0xffffffffu, other, o);
+    }
+    if (other || (count > 0 && count != last - first + 1)) return make_int2(kWinGeneral, 0);
+    return count == 0 ? make_int2(0, 0) : make_int2(first, last + 1);
 }
 
-// Chunk classes (2 bits per chunk) of one thread's chunks for a row: the mask
-// classes of the row's batch entry (cached: consecutive rows usually share
-// it), then, when causal, chunks wholly after the last visible key `qlim` are
-// skipped and the chunk holding it is mixed.
-template <typename T, int TPR, int CPT>
-struct RowClasses {
-    const T *mask;
-    int Tk, nchunk, lane;
-    int64_t mb = -1;
-    uint32_t mcls = 0u;
-    __device__ __forceinline__ RowClasses(const T *m, int tk, int lane_)
-        : mask(m), Tk(tk), nchunk(tk / Traits<T>::kVec), lane(lane_) {}
-    __device__ __forceinline__ uint32_t get(int64_t b, int64_t qlim, int causal) {
-        constexpr int V = Traits<T>::kVec;
-        uint32_t cls = 0u;
-        if (mask) {
-            if (b != mb) {
-                mb = b;
-                mcls = 0u;
-                const T *mrow = mask + b * (int64_t)Tk;
-#pragma unroll
-                for (int k = 0; k < CPT; ++k) {
-                    const int c = k * TPR + lane;
-                    if (c < nchunk)
-                        mcls |= mask_chunk_class<T>(ld_cached16(mrow + c * V)) << (2 * k);
-                }
-            }
-            cls = mcls;
-        }
-        if (causal) {
-#pragma unroll
-            for (int k = 0; k < CPT; ++k) {
-                const int64_t j0 = (int64_t)(k * TPR + lane) * V;
-                const uint32_t cur = (cls >> (2 * k)) & 3u;
-                uint32_t nc = cur;
-                if (j0 > qlim) nc = kChunkSkip;
-                else if (j0 + V - 1 > qlim && cur != kChunkSkip) nc = kChunkMixed;
-                cls = (cls & ~(3u << (2 * k))) | (nc << (2 * k));
-            }
-        }
-        return cls;
-    }
-};
-
-// Position (batch entry, query) of consecutive rows, advanced without
-// division: rows of a row group are contiguous.
-struct RowPos {
-    int64_t b = 0, rem = 0, q = 0;
-    __device__ __forceinline__ void init(int64_t row, int64_t rows_per_batch, int64_t Tq) {
-        b = row / rows_per_batch;
-        rem = row - b * rows_per_batch;
-        q = row % Tq;
-    }
-    __device__ __forceinline__ void next(int64_t rows_per_batch, int64_t Tq) {
-        if (++rem == rows_per_batch) {
-            rem = 0;
-            ++b;
-        }
-        if (++q == Tq) q = 0;
-    }
-};
-
-// Shared memory of softmax_fw_vec: S stages of CPT 16-byte chunks per thread,
-// plus one word of chunk-class bits per thread and stage.
+// Shared memory of softmax_fw_vec: S stages of CPT 16-byte chunks per
+// thread, plus each thread's (lo, hi) of the row in that stage.
 template <int TPR, int CPT, int S>
 constexpr size_t softmax_fw_smem() {
-    return (size_t)S * (TPR <= 32 ? 256 : TPR) * (CPT * 16 + 4);
+    return (size_t)S * (TPR <= 32 ? 256 : TPR) * (CPT * 16 + 8);
 }
 
 template <typename T, int TPR, int CPT, int S, bool SCALED>
@@ -137,39 +108,80 @@ softmax_fw_vec(T *out, const T *inp, const T *mask, int64_t rows,
     constexpr int H2 = V / 2;
     constexpr int BLOCK = TPR <= 32 ? 256 : TPR;
     constexpr int G = BLOCK / TPR;  // row groups per block
-    static_assert(2 * CPT <= 32, "class bits");
     extern __shared__ uint4 dsmem[];
-    uint4 *stage = dsmem;                                                  // [S][CPT][BLOCK]
-    uint32_t *clsb = reinterpret_cast<uint32_t *>(dsmem + S * CPT * BLOCK);  // [S][BLOCK]
+    uint4 *stage = dsmem;                                              // [S][CPT][BLOCK]
+    int2 *winb = reinterpret_cast<int2 *>(dsmem + S * CPT * BLOCK);    // [S][BLOCK]
     __shared__ float red[TPR > 32 ? 64 : 1];
+    __shared__ int2 wtab[kWinMax];
 
     const int tid = threadIdx.x;
     const int lane = tid % TPR;
     const int grp = tid / TPR;
-    const int nchunk = Tk / V;
     const int64_t ngroups = (int64_t)gridDim.x * G;
-    const int64_t per = (rows + ngroups - 1) / ngroups;  // rows per group (uniform)
+    const int per = (int)((rows + ngroups - 1) / ngroups);  // rows per group (uniform)
     const int64_t rbeg = ((int64_t)blockIdx.x * G + grp) * per;
     const int64_t rend = rbeg + per < rows ? rbeg + per : rows;
 
-    RowClasses<T, TPR, CPT> classes(mask, Tk, lane);
+    // Windows of the batch entries this block's rows belong to (one warp per
+    // entry).  A block spanning more than kWinMax entries treats every mask
+    // row as general.
+    const int64_t blk0 = (int64_t)blockIdx.x * G * per;
+    const int64_t b_first = blk0 < rows ? blk0 / rows_per_batch : 0;
+    bool general = false;
+    if (mask) {
+        const int64_t blk1 = min(rows, blk0 + (int64_t)G * per);
+        const int64_t nb = blk1 > blk0 ? (blk1 - 1) / rows_per_batch - b_first + 1 : 0;
+        if (nb > kWinMax) {
+            general = true;
+        } else {
+            for (int i = tid >> 5; i < nb; i += BLOCK / 32) {
+                const int2 w = mask_row_window<T, true>(mask + (b_first + i) * (int64_t)Tk, Tk);
+                if ((tid & 31) == 0) wtab[i] = w;
+            }
+            __syncthreads();
+        }
+    }
 
-    // Issue the copies of the next row into stage s (an empty group past the end).
-    RowPos ip;
-    if (rbeg < rend) ip.init(rbeg, rows_per_batch, Tq);
+    // Row cursor for issuing: batch entry (relative to the block's first),
+    // position in the batch entry and query index, advanced without
+    // division (the launcher keeps rows below 2^31, so they fit 32 bits).
+    const int rpb = (int)rows_per_batch, tq = (int)Tq, qo = (int)qoff;
+    int ib = 0, irem = 0, iq = 0;
+    if (rbeg < rend) {
+        const int64_t b = rbeg / rows_per_batch;
+        ib = (int)(b - b_first);
+        irem = (int)(rbeg - b * rows_per_batch);
+        iq = (int)(rbeg % Tq);
+    }
+    const T *xnext = inp + rbeg * (int64_t)Tk;
     int64_t inext = rbeg;
+    // Issue the copies of the next row's visible chunks into stage s and
+    // record the row's window (an empty group past the end).
     auto issue = [&](int s) {
         if (inext < rend) {
-            const uint32_t cls = classes.get(ip.b, ip.q + qoff, causal);
-            clsb[s * BLOCK + tid] = cls;
-            const T *xrow = inp + inext * (int64_t)Tk;
+            int lo = 0, hi = Tk;
+            if (general) {
+                lo = kWinGeneral;
+            } else if (mask) {
+                const int2 w = wtab[ib];
+                lo = w.x;
+                if (w.x != kWinGeneral) hi = w.y;
+            }
+            if (causal) hi = min(hi, iq + qo + 1);  // query iq sees keys j <= iq + qoff
+            winb[s * BLOCK + tid] = make_int2(lo, hi);
+            const int lo_ld = max(lo, 0);
 #pragma unroll
             for (int k = 0; k < CPT; ++k) {
-                const int c = k * TPR + lane;
-                if (c < nchunk && ((cls >> (2 * k)) & 3u) != kChunkSkip)
-                    cp_async16(&stage[(s * CPT + k) * BLOCK + tid], xrow + c * V);
+                const int j0 = (k * TPR + lane) * V;
+                if (j0 < hi && j0 + V > lo_ld)
+                    cp_async16(&stage[(s * CPT + k) * BLOCK + tid], xnext + j0);
             }
-            ip.next(rows_per_batch, Tq);
+            xnext += Tk;
+            if (++irem == rpb) {
+                irem = 0;
+                ++ib;
+            }
+            if (++iq == tq) iq = 0;
         }
         ++inext;
         cp_async_commit();
@@ -177,69 +189,67 @@ softmax_fw_vec(T *out, const T *inp, const T *mask, int64_t rows,
 #pragma unroll
     for (int s = 0; s < S - 1; ++s) issue(s);
 
-    RowPos cp;
-    if (rbeg < rend) cp.init(rbeg, rows_per_batch, Tq);
+    T *orow = out + rbeg * (int64_t)Tk;
     int s_cur = 0, s_iss = S - 1;
-    for (int64_t k = 0; k < per; ++k) {
+    for (int k = 0; k < per; ++k) {
         issue(s_iss);
         s_iss = s_iss + 1 == S ? 0 : s_iss + 1;
         cp_async_wait<S - 1>();  // this thread's copies of row k have landed
 
-        const int64_t row = rbeg + k;
-        const bool valid = row < rend;
-        const uint32_t ccls = valid ? clsb[s_cur * BLOCK + tid] : 0u;
-        const int qi = (valid && causal) ? (int)(cp.q + qoff) : Tk;  // last visible key
-        const T *mrow = (valid && mask) ? mask + cp.b * (int64_t)Tk : nullptr;
+        const bool valid = rbeg + k < rend;
+        const int2 w = valid ? winb[s_cur * BLOCK + tid] : make_int2(0, 0);
+        const bool gen = w.x == kWinGeneral;
+        const int lo = gen ? 0 : w.x, hi = w.y;
+        const T *mrow = nullptr;  // the mask row, general rows only
+        if (gen) mrow = mask + ((rbeg + k) / rows_per_batch) * (int64_t)Tk;
 
-        // SCALED: plain chunks keep x (their maximum mp is scaled once,
-        // below) and mixed chunks hold z = scale * x + mask; otherwise scale
-        // is 1 and every chunk holds z
+        // v holds x (window rows; SCALED: the maximum is scaled once below)
+        // or z = scale * x + mask (general rows); -inf on invisible keys
         float2 v[CPT][H2];
-        float m = -INFINITY, mp = -INFINITY;
+        float m = -INFINITY;
 #pragma unroll
         for (int kk = 0; kk < CPT; ++kk) {
-            const int c = kk * TPR + lane;
-            const uint32_t cls = (ccls >> (2 * kk)) & 3u;
-            if (valid && c < nchunk && cls != kChunkSkip) {
+            const int j0 = (kk * TPR + lane) * V;
+            if (j0 < hi && j0 + V > lo) {
                 unpack2<T>(stage[(s_cur * CPT + kk) * BLOCK + tid], v[kk]);
-                if (cls == kChunkMixed) {
+                if (gen) {
                     float2 mv[H2];
-#pragma unroll
-                    for (int h = 0; h < H2; ++h) mv[h] = f2(0.f);
-                    if (mrow) unpack2<T>(ld_cached16(mrow + c * V), mv);
+                    unpack2<T>(ld_cached16(mrow + j0), mv);
 #pragma unroll
                     for (int h = 0; h < H2; ++h) {
-                        const int j = c * V + 2 * h;
-                        if constexpr (SCALED) {
-                            v[kk][h].x = j > qi ? -INFINITY : fmaf(v[kk][h].x, scale, mv[h].x);
-                            v[kk][h].y = j + 1 > qi ? -INFINITY : fmaf(v[kk][h].y, scale, mv[h].y);
-                        } else {
-                            v[kk][h].x = j > qi ? -INFINITY : v[kk][h].x + mv[h].x;
-                            v[kk][h].y = j + 1 > qi ? -INFINITY : v[kk][h].y + mv[h].y;
-                        }
+                        // keys masked with -inf or in the causal future are
+                        // -inf whatever their score
+                        const int j = j0 + 2 * h;
+                        const float zx = SCALED ? fmaf(v[kk][h].x, scale, mv[h].x)
+                                                : v[kk][h].x + mv[h].x;
+                        const float zy = SCALED ? fmaf(v[kk][h].y, scale, mv[h].y)
+                                                : v[kk][h].y + mv[h].y;
+                        v[kk][h].x = (j < hi && mv[h].x != -INFINITY) ? zx : -INFINITY;
+                        v[kk][h].y = (j + 1 < hi && mv[h].y != -INFINITY) ? zy : -INFINITY;
                     }
+                } else if (j0 < lo || j0 + V > hi) {
 #pragma unroll
-                    for (int h = 0; h < H2; ++h) m = fmax3(m, v[kk][h].x, v[kk][h].y);
-                } else {
-#pragma unroll
-                    for (int h = 0; h < H2; ++h) mp = fmax3(mp, v[kk][h].x, v[kk][h].y);
+                    for (int h = 0; h < H2; ++h) {
+                        const int j = j0 + 2 * h;
+                        if (j < lo || j >= hi) v[kk][h].x = -INFINITY;
+                        if (j + 1 < lo || j + 1 >= hi) v[kk][h].y = -INFINITY;
+                    }
                 }
+#pragma unroll
+                for (int h = 0; h < H2; ++h) m = fmax3(m, v[kk][h].x, v[kk][h].y);
             }
         }
-        // scale > 0: the maximum of scale * x is scale * mp
-        m = fmaxf(m, SCALED ? mp * scale : mp);
         m = group_reduce<TPR, OpMax>(m, red);
-        // e = 2^(z*log2e - m*log2e), z*log2e taken as x*(scale*log2e) on plain
-        // chunks; a row with no visible key sums to 0
-        const float mL = m == -INFINITY ? 0.f : m * kLog2e;
-        const float sl2 = SCALED ? scale * kLog2e : kLog2e;
+        // e = 2^(v * mul - m * log2e); window rows of the scaled softmax hold
+        // x, whose maximum times scale (> 0) is the maximum of scale * x
+        if (SCALED && !gen) m *= scale;
+        const float mL = m == -INFINITY ? 0.f : m * kLog2e;  // a row with no visible key sums to 0
+        const float2 mul = f2(SCALED && !gen ? scale * kLog2e : kLog2e);
         float2 sum2 = f2(0.f);
 #pragma unroll
         for (int kk = 0; kk < CPT; ++kk) {
-            const int c = kk * TPR + lane;
-            const uint32_t cls = (ccls >> (2 * kk)) & 3u;
-            if (valid && c < nchunk && cls != kChunkSkip) {
-                const float2 mul = f2((!SCALED || cls == kChunkMixed) ? kLog2e : sl2);
+            const int j0 = (kk * TPR + lane) * V;
+            if (j0 < hi && j0 + V > lo) {
 #pragma unroll
                 for (int h = 0; h < H2; ++h) {
                     float2 t = fma2(v[kk][h], mul, f2(-mL));
@@ -251,22 +261,25 @@ softmax_fw_vec(T *out, const T *inp, const T *mask, int64_t rows,
             }
         }
         const float sum = group_reduce<TPR, OpSum>(sum2.x + sum2.y, red);
-        const float2 inv = f2(sum > 0.f ? 1.f / sum : 0.f);
+        const float2 inv = f2(sum > 0.f ? fast_rcp(sum) : 0.f);
 
-        T *orow = out + row * (int64_t)Tk;
+        if (valid) {
 #pragma unroll
-        for (int kk = 0; kk < CPT; ++kk) {
-            const int c = kk * TPR + lane;
-            const uint32_t cls = (ccls >> (2 * kk)) & 3u;
-            if (valid && c < nchunk) {
-                float2 yv[H2];
+            for (int kk = 0; kk < CPT; ++kk) {
+                const int j0 = (kk * TPR + lane) * V;
+                if (j0 < Tk) {
+                    uint4 o = make_uint4(0u, 0u, 0u, 0u);
+                    if (j0 < hi && j0 + V > lo) {
+                        float2 yv[H2];
 #pragma unroll
-                for (int h = 0; h < H2; ++h)
-                    yv[h] = cls == kChunkSkip ? f2(0.f) : mul2(v[kk][h], inv);
-                st_stream16(orow + c * V, pack2<T>(yv));
+                        for (int h = 0; h < H2; ++h) yv[h] = mul2(v[kk][h], inv);
+                        o = pack2<T>(yv);
+                    }
+                    st_stream16(orow + j0, o);
+                }
             }
         }
-        if (valid) cp.next(rows_per_batch, Tq);
+        orow += Tk;
         s_cur = s_cur + 1 == S ? 0 : s_cur + 1;
     }
 }
@@ -420,14 +433,17 @@ softmax_bw_loop(T *dinp, const T *dout, const T *y, int64_t rows, int64_t Tk) {
 
 // ----------------------------------------------------------------------------
 // Masked backward: dinp_j = scale * y_j (dout_j - sum over visible k of
-// y_k dout_k) on visible keys, 0 elsewhere.  Chunks whose keys are all
-// invisible (mask -inf, or causal future) are neither read nor summed; they
-// are written as zeros.  This form serves rows of up to three chunks per
-// thread: same row mapping as softmax_bw_vec (rows strided over the grid);
-// each row finds its batch entry and query by division and classifies its
-// mask chunks afresh (the mask row stays in L1), so nothing is carried from
-// row to row and the kernel stays near the plain backward's register budget
-// and occupancy.  Longer rows take softmax_bw_masked_runs below.
+// y_k dout_k) on visible keys, 0 elsewhere.  A key is visible when its mask
+// element is not -inf and, when causal, it is not in the query's future.
+// As in the forward, each block first finds the window [lo, hi) of visible
+// keys of every batch entry it touches (mask rows whose visible keys are not
+// contiguous are "general": their rows test the mask element by element),
+// and each row group takes a contiguous run of rows, its position advanced
+// without division.  Chunks with no visible key are neither read nor summed
+// and are written as zeros; only the chunks straddling lo or hi (and every
+// chunk of a general row) select element by element.  Rows are loaded
+// straight into registers (y and dout, CPT chunks each), as in the plain
+// backward.
 // ----------------------------------------------------------------------------
 template <typename T, int TPR, int CPT>
 __global__ void __launch_bounds__(TPR <= 32 ? 256 : TPR)
@@ -441,201 +457,137 @@ softmax_bw_masked_vec(T *dinp, const T *dout, const T *y, const T *mask, int64_t
     constexpr int BLOCK = TPR <= 32 ? 256 : TPR;
     constexpr int G = BLOCK / TPR;
     __shared__ float red[TPR > 32 ? 64 : 1];
+    __shared__ int2 wtab[kWinMax];
 
-    const int lane = threadIdx.x % TPR;
-    const int grp = threadIdx.x / TPR;
-    const int nchunk = Tk / V;
-    const bool narrow = rows <= INT32_MAX && rows_per_batch <= INT32_MAX && Tq <= INT32_MAX;
+    const int tid = threadIdx.x;
+    const int lane = tid % TPR;
+    const int grp = tid / TPR;
+    const int64_t ngroups = (int64_t)gridDim.x * G;
+    const int per = (int)((rows + ngroups - 1) / ngroups);
+    const int64_t rbeg = ((int64_t)blockIdx.x * G + grp) * per;
+    const int64_t rend = rbeg + per < rows ? rbeg + per : rows;
 
-    for (int64_t base = (int64_t)blockIdx.x * G; base < rows;
-         base += (int64_t)gridDim.x * G) {
-        const int64_t row = base + grp;
-        const bool valid = row < rows;
-        const int64_t off = row * (int64_t)Tk;
-        // batch entry and last visible key of this row
-        int64_t b = 0, q = 0;
-        if (valid && (mask || causal)) {
-            if (narrow) {
-                const uint32_t r32 = (uint32_t)row;
-                b = r32 / (uint32_t)rows_per_batch;
-                q = causal ? r32 % (uint32_t)Tq : 0;
-            } else {
-                b = row / rows_per_batch;
-                q = causal ? row % Tq : 0;
+    const int64_t blk0 = (int64_t)blockIdx.x * G * per;
+    const int64_t b_first = blk0 < rows ? blk0 / rows_per_batch : 0;
+    bool general = false;
+    if (mask) {
+        const int64_t blk1 = min(rows, blk0 + (int64_t)G * per);
+        const int64_t nb = blk1 > blk0 ? (blk1 - 1) / rows_per_batch - b_first + 1 : 0;
+        if (nb > kWinMax) {
+            general = true;
+        } else {
+            for (int i = tid >> 5; i < nb; i += BLOCK / 32) {
+                const int2 w = mask_row_window<T, false>(mask + (b_first + i) * (int64_t)Tk, Tk);
+                if ((tid & 31) == 0) wtab[i] = w;
+            }
+            __syncthreads();
+        }
+    }
+
+    const int rpb = (int)rows_per_batch, tq = (int)Tq, qo = (int)qoff;
+    int ib = 0, irem = 0, iq = 0;
+    if (rbeg < rend) {
+        const int64_t b = rbeg / rows_per_batch;
+        ib = (int)(b - b_first);
+        irem = (int)(rbeg - b * rows_per_batch);
+        iq = (int)(rbeg % Tq);
+    }
+    const int64_t off0 = rbeg * (int64_t)Tk;
+    const T *yrow = y + off0;
+    const T *grow = dout + off0;
+    T *drow = dinp + off0;
+    for (int k = 0; k < per; ++k) {
+        const bool valid = rbeg + k < rend;
+        int lo = 0, hi = valid ? Tk : 0;
+        bool gen = general;
+        if (valid && mask && !general) {
+            const int2 w = wtab[ib];
+            gen = w.x == kWinGeneral;
+            if (!gen) {
+                lo = w.x;
+                hi = w.y;
             }
         }
-        const int64_t qi = causal ? q + qoff : (int64_t)Tk;
-        const T *mrow = (valid && mask) ? mask + b * (int64_t)Tk : nullptr;
+        if (valid && causal) hi = min(hi, iq + qo + 1);
+        const T *mrow = gen ? mask + ((rbeg + k) / rows_per_batch) * (int64_t)Tk : nullptr;
 
         uint4 yr[CPT], gr[CPT];
-        uint32_t vis[CPT];  // visible elements of each chunk (bit e)
+        uint32_t part = 0u;  // bit kk: chunk kk is only partly visible
 #pragma unroll
         for (int kk = 0; kk < CPT; ++kk) {
-            const int c = kk * TPR + lane;
+            const int j0 = (kk * TPR + lane) * V;
             yr[kk] = gr[kk] = make_uint4(0u, 0u, 0u, 0u);
-            vis[kk] = 0u;
-            if (!valid || c >= nchunk) continue;
-            uint32_t bits = (1u << V) - 1u;
-            if (mrow) {
-                float mv[V];
-                Tr::unpack(ld_cached16(mrow + c * V), mv);
-                bits = 0u;
-#pragma unroll
-                for (int e = 0; e < V; ++e) bits |= (mv[e] != -INFINITY ? 1u : 0u) << e;
-            }
-            if (causal) {
-                const int64_t j0 = (int64_t)c * V;
-#pragma unroll
-                for (int e = 0; e < V; ++e)
-                    if (j0 + e > qi) bits &= ~(1u << e);
-            }
-            vis[kk] = bits;
-            if (bits) {
-                yr[kk] = ld_stream16(y + off + c * V);
-                gr[kk] = ld_stream16(dout + off + c * V);
+            if (j0 < hi && j0 + V > lo) {
+                yr[kk] = ld_stream16(yrow + j0);
+                gr[kk] = ld_stream16(grow + j0);
+                if (gen || j0 < lo || j0 + V > hi) part |= 1u << kk;
             }
         }
         float2 s2 = f2(0.f);
+        uint32_t vis[CPT];  // partly visible chunks: visible elements (bit e)
 #pragma unroll
         for (int kk = 0; kk < CPT; ++kk) {
+            const int j0 = (kk * TPR + lane) * V;
             float2 yv[H2], gv[H2];
             unpack2<T>(yr[kk], yv);
             unpack2<T>(gr[kk], gv);
-            if (vis[kk] == (1u << V) - 1u) {
-#pragma unroll
-                for (int h = 0; h < H2; ++h) s2 = fma2(yv[h], gv[h], s2);
-            } else {
-#pragma unroll
-                for (int h = 0; h < H2; ++h) {
-                    const float2 p = mul2(yv[h], gv[h]);
-                    s2.x += (vis[kk] >> (2 * h)) & 1u ? p.x : 0.f;
-                    s2.y += (vis[kk] >> (2 * h + 1)) & 1u ? p.y : 0.f;
-                }
-            }
-        }
-        const float s = group_reduce<TPR, OpSum>(s2.x + s2.y, red);
-#pragma unroll
-        for (int kk = 0; kk < CPT; ++kk) {
-            const int c = kk * TPR + lane;
-            if (valid && c < nchunk) {
-                float2 yv[H2], gv[H2], dv[H2];
-                unpack2<T>(yr[kk], yv);
-                unpack2<T>(gr[kk], gv);
-#pragma unroll
-                for (int h = 0; h < H2; ++h) {
-                    // scale * y * (g - s), with scale folded into the difference
-                    const float2 t = mul2(yv[h], fma2(gv[h], f2(scale), f2(-s * scale)));
-                    dv[h].x = (vis[kk] >> (2 * h)) & 1u ? t.x : 0.f;
-                    dv[h].y = (vis[kk] >> (2 * h + 1)) & 1u ? t.y : 0.f;
-                }
-                st_stream16(dinp + off + c * V, pack2<T>(dv));
-            }
-        }
-    }
-}
-
-// ----------------------------------------------------------------------------
-// Masked backward for rows of four or more chunks per thread: each row group
-// takes a contiguous run of rows, so the mask chunk classes are cached per
-// batch entry (RowClasses) and the row position advances without division
-// (RowPos); per-element visibility is kept for every chunk.
-// ----------------------------------------------------------------------------
-template <typename T, int TPR, int CPT>
-__global__ void __launch_bounds__(TPR <= 32 ? 256 : TPR)
-softmax_bw_masked_runs(T *dinp, const T *dout, const T *y, const T *mask, int64_t rows,
-                      int64_t rows_per_batch, int64_t Tq, int Tk, int causal, int64_t qoff,
-                      float scale) {
-    pdl_begin();
-    using Tr = Traits<T>;
-    constexpr int V = Tr::kVec;
-    constexpr int H2 = V / 2;
-    constexpr int BLOCK = TPR <= 32 ? 256 : TPR;
-    constexpr int G = BLOCK / TPR;
-    __shared__ float red[TPR > 32 ? 64 : 1];
-
-    const int lane = threadIdx.x % TPR;
-    const int grp = threadIdx.x / TPR;
-    const int nchunk = Tk / V;
-    const int64_t ngroups = (int64_t)gridDim.x * G;
-    const int64_t per = (rows + ngroups - 1) / ngroups;
-    const int64_t rbeg = ((int64_t)blockIdx.x * G + grp) * per;
-    const int64_t rend = rbeg + per < rows ? rbeg + per : rows;
-    RowClasses<T, TPR, CPT> classes(mask, Tk, lane);
-    RowPos pos;
-    if (rbeg < rend) pos.init(rbeg, rows_per_batch, Tq);
-
-    for (int64_t k = 0; k < per; ++k) {
-        const int64_t row = rbeg + k;
-        const bool valid = row < rend;
-        const int64_t off = row * (int64_t)Tk;
-        const uint32_t ccls = valid ? classes.get(pos.b, pos.q + qoff, causal) : 0u;
-        const int qi = (valid && causal) ? (int)(pos.q + qoff) : Tk;
-        const T *mrow = (valid && mask) ? mask + pos.b * (int64_t)Tk : nullptr;
-
-        uint4 yr[CPT], gr[CPT];
-#pragma unroll
-        for (int kk = 0; kk < CPT; ++kk) {
-            const int c = kk * TPR + lane;
-            const uint32_t cls = (ccls >> (2 * kk)) & 3u;
-            if (valid && c < nchunk && cls != kChunkSkip) {
-                yr[kk] = ld_stream16(y + off + c * V);
-                gr[kk] = ld_stream16(dout + off + c * V);
-            } else {
-                yr[kk] = make_uint4(0u, 0u, 0u, 0u);
-                gr[kk] = make_uint4(0u, 0u, 0u, 0u);
-            }
-        }
-        // visibility of the elements of mixed chunks (mask -inf or future)
-        uint32_t vis[CPT];
-#pragma unroll
-        for (int kk = 0; kk < CPT; ++kk) {
-            const int c = kk * TPR + lane;
-            const uint32_t cls = (ccls >> (2 * kk)) & 3u;
-            vis[kk] = cls == kChunkSkip ? 0u : (1u << V) - 1u;
-            if (valid && c < nchunk && cls == kChunkMixed) {
+            vis[kk] = (1u << V) - 1u;
+            if (part & (1u << kk)) {
+                uint32_t bits = 0u;
                 float mv[V];
 #pragma unroll
                 for (int e = 0; e < V; ++e) mv[e] = 0.f;
-                if (mrow) Tr::unpack(ld_cached16(mrow + c * V), mv);
-                uint32_t bits = 0u;
+                if (gen) Tr::unpack(ld_cached16(mrow + j0), mv);
 #pragma unroll
                 for (int e = 0; e < V; ++e)
-                    if (mv[e] != -INFINITY && c * V + e <= qi) bits |= 1u << e;
+                    if (j0 + e >= lo && j0 + e < hi && mv[e] != -INFINITY) bits |= 1u << e;
                 vis[kk] = bits;
-            }
-        }
-        float2 s2 = f2(0.f);
 #pragma unroll
-        for (int kk = 0; kk < CPT; ++kk) {
-            float2 yv[H2], gv[H2];
-            unpack2<T>(yr[kk], yv);
-            unpack2<T>(gr[kk], gv);
+                for (int h = 0; h < H2; ++h) {
+                    const float2 p = mul2(yv[h], gv[h]);
+                    s2.x += (bits >> (2 * h)) & 1u ? p.x : 0.f;
+                    s2.y += (bits >> (2 * h + 1)) & 1u ? p.y : 0.f;
+                }
+            } else {
+                // fully visible, or not loaded (zeros)
 #pragma unroll
-            for (int h = 0; h < H2; ++h) {
-                const float2 p = mul2(yv[h], gv[h]);
-                s2.x += (vis[kk] >> (2 * h)) & 1u ? p.x : 0.f;
-                s2.y += (vis[kk] >> (2 * h + 1)) & 1u ? p.y : 0.f;
+                for (int h = 0; h < H2; ++h) s2 = fma2(yv[h], gv[h], s2);
             }
         }
         const float s = group_reduce<TPR, OpSum>(s2.x + s2.y, red);
+        if (valid) {
 #pragma unroll
-        for (int kk = 0; kk < CPT; ++kk) {
-            const int c = kk * TPR + lane;
-            if (valid && c < nchunk) {
-                float2 yv[H2], gv[H2], dv[H2];
-                unpack2<T>(yr[kk], yv);
-                unpack2<T>(gr[kk], gv);
+            for (int kk = 0; kk < CPT; ++kk) {
+                const int j0 = (kk * TPR + lane) * V;
+                if (j0 < Tk) {
+                    uint4 o = make_uint4(0u, 0u, 0u, 0u);
+                    if (j0 < hi && j0 + V > lo) {
+                        float2 yv[H2], gv[H2], dv[H2];
+                        unpack2<T>(yr[kk], yv);
+                        unpack2<T>(gr[kk], gv);
 #pragma unroll
-                for (int h = 0; h < H2; ++h) {
-                    // scale * y * (g - s), with scale folded into the difference
-                    const float2 t = mul2(yv[h], fma2(gv[h], f2(scale), f2(-s * scale)));
-                    dv[h].x = (vis[kk] >> (2 * h)) & 1u ? t.x : 0.f;
-                    dv[h].y = (vis[kk] >> (2 * h + 1)) & 1u ? t.y : 0.f;
+                        for (int h = 0; h < H2; ++h) {
+                            // scale * y * (g - s), scale folded into the difference
+                            dv[h] = mul2(yv[h], fma2(gv[h], f2(scale), f2(-s * scale)));
+                            if (part & (1u << kk)) {
+                                dv[h].x = (vis[kk] >> (2 * h)) & 1u ? dv[h].x : 0.f;
+                                dv[h].y = (vis[kk] >> (2 * h + 1)) & 1u ? dv[h].y : 0.f;
+                            }
+                        }
+                        o = pack2<T>(dv);
+                    }
+                    st_stream16(drow + j0, o);
                 }
-                st_stream16(dinp + off + c * V, pack2<T>(dv));
             }
+            if (++irem == rpb) {
+                irem = 0;
+                ++ib;
+            }
+            if (++iq == tq) iq = 0;
         }
-        if (valid) pos.next(rows_per_batch, Tq);
+        yrow += Tk;
+        grow += Tk;
+        drow += Tk;
     }
 }
 
