@@ -445,8 +445,65 @@ softmax_bw_loop(T *dinp, const T *dout, const T *y, int64_t rows, int64_t Tk) {
 // straight into registers (y and dout, CPT chunks each), as in the plain
 // backward.
 // ----------------------------------------------------------------------------
+// Bit mask (one bit per element of a 16-byte chunk of V keys starting at
+// key j0) of the visible keys: inside [lo, hi) and, for a general row (mrow
+// = its mask row, else nullptr), with a mask element that is not -inf.
+template <typename T>
+__device__ __forceinline__ uint32_t chunk_visible_bits(const T *mrow, int j0, int lo, int hi) {
+    using Tr = Traits<T>;
+    constexpr int V = Tr::kVec;
+    uint32_t bits = 0u;
+#pragma unroll
+    for (int e = 0; e < V; ++e) bits |= (j0 + e >= lo && j0 + e < hi ? 1u : 0u) << e;
+    if (mrow) {
+        float mv[V];
+        Tr::unpack(ld_cached16(mrow + j0), mv);
+#pragma unroll
+        for (int e = 0; e < V; ++e)
+            if (mv[e] == -INFINITY) bits &= ~(1u << e);
+    }
+    return bits;
+}
+
+// AND mask of the 32-bit word w of a 16-byte chunk that keeps the elements
+// whose bits are set in `bits` and clears the others (to +0).
+template <typename T>
+__device__ __forceinline__ uint32_t keep_word(uint32_t bits, int w) {
+    if constexpr (Traits<T>::kVec == 4) {
+        return (bits >> w) & 1u ? 0xffffffffu : 0u;
+    } else {
+        return ((bits >> (2 * w)) & 1u ? 0x0000ffffu : 0u) |
+               ((bits >> (2 * w + 1)) & 1u ? 0xffff0000u : 0u);
+    }
+}
+template <typename T>
+__device__ __forceinline__ void keep_elements(uint4 &u, uint32_t bits) {
+    u.x &= keep_word<T>(bits, 0);
+    u.y &= keep_word<T>(bits, 1);
+    u.z &= keep_word<T>(bits, 2);
+    u.w &= keep_word<T>(bits, 3);
+}
+
+// Masked backward: dinp_j = scale * y_j (dout_j - sum over visible k of
+// y_k dout_k) on visible keys, 0 elsewhere.  A key is visible when its mask
+// element is not -inf and, when causal, it is not in the query's future.
+// The plain backward's structure (y and dout straight into registers, CPT
+// chunks each, one fused multiply-add per element pair for the sum) with the
+// forward's windows: each block first finds the window [lo, hi) of visible
+// keys of every batch entry it touches (mask rows whose visible keys are not
+// contiguous are "general"), each row group takes a contiguous run of rows
+// and advances its position without division.  Chunks with no visible key
+// are neither read nor summed and are written as zeros; in the chunks that
+// straddle lo or hi (every chunk of a general row) the invisible elements of
+// y and dout are cleared to 0 before the arithmetic, so they add nothing to
+// the sum and their output is 0, whatever the memory held there.
+template <int TPR, int CPT>
+constexpr int softmax_bw_masked_min_blocks() {
+    return TPR <= 32 ? (CPT <= 1 ? 5 : CPT <= 2 ? 4 : CPT <= 3 ? 3 : CPT <= 6 ? 2 : 1) : 1;
+}
+
 template <typename T, int TPR, int CPT>
-__global__ void __launch_bounds__(TPR <= 32 ? 256 : TPR)
+__global__ void __launch_bounds__(TPR <= 32 ? 256 : TPR, (softmax_bw_masked_min_blocks<TPR, CPT>()))
 softmax_bw_masked_vec(T *dinp, const T *dout, const T *y, const T *mask, int64_t rows,
                       int64_t rows_per_batch, int64_t Tq, int Tk, int causal, int64_t qoff,
                       float scale) {
@@ -465,7 +522,7 @@ softmax_bw_masked_vec(T *dinp, const T *dout, const T *y, const T *mask, int64_t
     const int64_t ngroups = (int64_t)gridDim.x * G;
     const int per = (int)((rows + ngroups - 1) / ngroups);
     const int64_t rbeg = ((int64_t)blockIdx.x * G + grp) * per;
-    const int64_t rend = rbeg + per < rows ? rbeg + per : rows;
+    const int nrow = (int)max((int64_t)0, min((int64_t)per, rows - rbeg));  // this group's rows
 
     const int64_t blk0 = (int64_t)blockIdx.x * G * per;
     const int64_t b_first = blk0 < rows ? blk0 / rows_per_batch : 0;
@@ -484,110 +541,77 @@ softmax_bw_masked_vec(T *dinp, const T *dout, const T *y, const T *mask, int64_t
         }
     }
 
-    const int rpb = (int)rows_per_batch, tq = (int)Tq, qo = (int)qoff;
     int ib = 0, irem = 0, iq = 0;
-    if (rbeg < rend) {
+    if (nrow > 0) {
         const int64_t b = rbeg / rows_per_batch;
         ib = (int)(b - b_first);
         irem = (int)(rbeg - b * rows_per_batch);
         iq = (int)(rbeg % Tq);
     }
-    const int64_t off0 = rbeg * (int64_t)Tk;
-    const T *yrow = y + off0;
-    const T *grow = dout + off0;
-    T *drow = dinp + off0;
-    for (int k = 0; k < per; ++k) {
-        const bool valid = rbeg + k < rend;
+    const int j_lane = lane * V;
+    int64_t off = rbeg * (int64_t)Tk;
+    for (int k = 0; k < per; ++k, off += Tk) {
+        const bool valid = k < nrow;
         int lo = 0, hi = valid ? Tk : 0;
-        bool gen = general;
-        if (valid && mask && !general) {
-            const int2 w = wtab[ib];
-            gen = w.x == kWinGeneral;
-            if (!gen) {
+        const T *mrow = nullptr;  // general rows test the mask element by element
+        if (valid && mask) {
+            const int2 w = general ? make_int2(kWinGeneral, 0) : wtab[ib];
+            if (w.x == kWinGeneral) {
+                mrow = mask + (b_first + ib) * (int64_t)Tk;
+            } else {
                 lo = w.x;
                 hi = w.y;
             }
         }
-        if (valid && causal) hi = min(hi, iq + qo + 1);
-        const T *mrow = gen ? mask + ((rbeg + k) / rows_per_batch) * (int64_t)Tk : nullptr;
+        if (valid && causal) hi = min(hi, iq + (int)qoff + 1);
 
         uint4 yr[CPT], gr[CPT];
-        uint32_t part = 0u;  // bit kk: chunk kk is only partly visible
 #pragma unroll
         for (int kk = 0; kk < CPT; ++kk) {
-            const int j0 = (kk * TPR + lane) * V;
+            const int j0 = kk * TPR * V + j_lane;
             yr[kk] = gr[kk] = make_uint4(0u, 0u, 0u, 0u);
             if (j0 < hi && j0 + V > lo) {
-                yr[kk] = ld_stream16(yrow + j0);
-                gr[kk] = ld_stream16(grow + j0);
-                if (gen || j0 < lo || j0 + V > hi) part |= 1u << kk;
+                yr[kk] = ld_stream16(y + off + j0);
+                gr[kk] = ld_stream16(dout + off + j0);
+                if (mrow || j0 < lo || j0 + V > hi) {
+                    const uint32_t bits = chunk_visible_bits<T>(mrow, j0, lo, hi);
+                    keep_elements<T>(yr[kk], bits);
+                    keep_elements<T>(gr[kk], bits);
+                }
             }
         }
         float2 s2 = f2(0.f);
-        uint32_t vis[CPT];  // partly visible chunks: visible elements (bit e)
 #pragma unroll
         for (int kk = 0; kk < CPT; ++kk) {
-            const int j0 = (kk * TPR + lane) * V;
             float2 yv[H2], gv[H2];
             unpack2<T>(yr[kk], yv);
             unpack2<T>(gr[kk], gv);
-            vis[kk] = (1u << V) - 1u;
-            if (part & (1u << kk)) {
-                uint32_t bits = 0u;
-                float mv[V];
 #pragma unroll
-                for (int e = 0; e < V; ++e) mv[e] = 0.f;
-                if (gen) Tr::unpack(ld_cached16(mrow + j0), mv);
-#pragma unroll
-                for (int e = 0; e < V; ++e)
-                    if (j0 + e >= lo && j0 + e < hi && mv[e] != -INFINITY) bits |= 1u << e;
-                vis[kk] = bits;
-#pragma unroll
-                for (int h = 0; h < H2; ++h) {
-                    const float2 p = mul2(yv[h], gv[h]);
-                    s2.x += (bits >> (2 * h)) & 1u ? p.x : 0.f;
-                    s2.y += (bits >> (2 * h + 1)) & 1u ? p.y : 0.f;
-                }
-            } else {
-                // fully visible, or not loaded (zeros)
-#pragma unroll
-                for (int h = 0; h < H2; ++h) s2 = fma2(yv[h], gv[h], s2);
-            }
+            for (int h = 0; h < H2; ++h) s2 = fma2(yv[h], gv[h], s2);
         }
         const float s = group_reduce<TPR, OpSum>(s2.x + s2.y, red);
         if (valid) {
+            const float2 sc = f2(scale), nss = f2(-s * scale);
 #pragma unroll
             for (int kk = 0; kk < CPT; ++kk) {
-                const int j0 = (kk * TPR + lane) * V;
+                const int j0 = kk * TPR * V + j_lane;
                 if (j0 < Tk) {
-                    uint4 o = make_uint4(0u, 0u, 0u, 0u);
-                    if (j0 < hi && j0 + V > lo) {
-                        float2 yv[H2], gv[H2], dv[H2];
-                        unpack2<T>(yr[kk], yv);
-                        unpack2<T>(gr[kk], gv);
+                    float2 yv[H2], gv[H2], dv[H2];
+                    unpack2<T>(yr[kk], yv);
+                    unpack2<T>(gr[kk], gv);
+                    // scale * y * (g - s), scale folded into the difference;
+                    // cleared elements give y = 0, hence 0 (of either sign)
 #pragma unroll
-                        for (int h = 0; h < H2; ++h) {
-                            // scale * y * (g - s), scale folded into the difference
-                            dv[h] = mul2(yv[h], fma2(gv[h], f2(scale), f2(-s * scale)));
-                            if (part & (1u << kk)) {
-                                dv[h].x = (vis[kk] >> (2 * h)) & 1u ? dv[h].x : 0.f;
-                                dv[h].y = (vis[kk] >> (2 * h + 1)) & 1u ? dv[h].y : 0.f;
-                            }
-                        }
-                        o = pack2<T>(dv);
-                    }
-                    st_stream16(drow + j0, o);
+                    for (int h = 0; h < H2; ++h) dv[h] = mul2(yv[h], fma2(gv[h], sc, nss));
+                    st_stream16(dinp + off + j0, pack2<T>(dv));
                 }
             }
-            if (++irem == rpb) {
+            if (++irem == (int)rows_per_batch) {
                 irem = 0;
                 ++ib;
             }
-            if (++iq == tq) iq = 0;
+            if (++iq == (int)Tq) iq = 0;
         }
-        yrow += Tk;
-        grow += Tk;
-        drow += Tk;
     }
 }
 
