@@ -822,14 +822,15 @@ ln_dgdb_staged(float *part, const T *dy, const T *x, const float *mean, const fl
 
 // ----------------------------------------------------------------------------
 // gamma / beta gradient, stage 2: sum the chunk partials in a fixed order.
-// Block = 32 columns x 32 chunk lanes; chunk lane t sums chunks t, t+32, ...
-// in increasing order, loading a batch of 8 of them at once (the kernel is
-// latency-bound: few bytes, many dependent rounds otherwise); the 32 lane
-// sums are then added in lane order.  nchunks == 0 writes zeros.
+// Block = 8 columns x 32 chunk lanes; chunk lane t sums chunks t, t+32, ...
+// in increasing order, loading a batch of 16 of them at once (the kernel is
+// latency-bound: few bytes, many dependent rounds otherwise; 16 covers the
+// at most 456 chunks in one round); the 32 lane sums are then added in lane
+// order.  nchunks == 0 writes zeros.
 // ----------------------------------------------------------------------------
-constexpr int kFinalCols = 32;
+constexpr int kFinalCols = 8;
 constexpr int kFinalLanes = 32;
-constexpr int kFinalBatch = 8;
+constexpr int kFinalBatch = 16;
 
 static __global__ void __launch_bounds__(kFinalCols * kFinalLanes)
 ln_dgdb_final(float *dgamma, float *dbeta, const float *part, int64_t nchunks, int64_t N) {

@@ -287,8 +287,16 @@ softmax_fw_vec(T *out, const T *inp, const T *mask, int64_t rows,
 // ----------------------------------------------------------------------------
 // Register-resident backward: dinp = y * (dout - sum(y * dout)).
 // ----------------------------------------------------------------------------
+// The three-chunk bucket is compiled for three resident 256-thread blocks
+// (up to 85 registers): left to its own heuristic ptxas keeps it at 64
+// registers with a spill.  0 leaves the other buckets to that heuristic
+// (as if no minimum were given; an explicit 1 would let ptxas take more
+// registers than the heuristic picks).
+template <int TPR, int CPT>
+constexpr int softmax_bw_min_blocks() { return TPR <= 32 && CPT == 3 ? 3 : 0; }
+
 template <typename T, int TPR, int CPT>
-__global__ void __launch_bounds__(TPR <= 32 ? 256 : TPR)
+__global__ void __launch_bounds__(TPR <= 32 ? 256 : TPR, (softmax_bw_min_blocks<TPR, CPT>()))
 softmax_bw_vec(T *dinp, const T *dout, const T *y, int64_t rows, int Tk) {
     pdl_begin();
     using Tr = Traits<T>;
@@ -497,9 +505,14 @@ __device__ __forceinline__ void keep_elements(uint4 &u, uint32_t bits) {
 // straddle lo or hi (every chunk of a general row) the invisible elements of
 // y and dout are cleared to 0 before the arithmetic, so they add nothing to
 // the sum and their output is 0, whatever the memory held there.
+//
+// Resident 256-thread blocks per SM asked of ptxas: four for the two-chunk
+// bucket (64 registers; left alone ptxas keeps the unpacked rows live across
+// the reduction and takes 96, five spill), fewer for wider rows, and 0 (its
+// own heuristic) where a cap would spill.
 template <int TPR, int CPT>
 constexpr int softmax_bw_masked_min_blocks() {
-    return TPR <= 32 ? (CPT <= 1 ? 5 : CPT <= 2 ? 4 : CPT <= 3 ? 3 : CPT <= 6 ? 2 : 1) : 1;
+    return TPR <= 32 ? (CPT <= 1 ? 5 : CPT <= 2 ? 4 : CPT <= 3 ? 3 : CPT <= 6 ? 2 : 0) : 0;
 }
 
 template <typename T, int TPR, int CPT>

@@ -306,8 +306,8 @@ class PipelinedPasses:
     """Passes fed from pinned host memory with the copies overlapped.
 
     Two device copies of the pass's buffers (``paths[0]`` and ``paths[1]``);
-    step k uses copy k % 2 (its kernels as ``run_overlapped`` schedules
-    them).  The host-to-device copies, the kernels and the
+    step k uses copy k % 2 (its kernels one after the other on one stream, as
+    ``run`` issues them).  The host-to-device copies, the kernels and the
     device-to-host copies run on their own streams; each copy direction is
     split over ``lanes`` streams (tensors dealt out largest first), so that
     several copy engines work at once.  Events order step k's upload after
@@ -325,7 +325,6 @@ class PipelinedPasses:
         self.hin, self.hout = paths[0].host_buffers()
         self.s_up = [torch.cuda.Stream(self.dev) for _ in range(lanes)]
         self.s_run = torch.cuda.Stream(self.dev)
-        self.s_side = torch.cuda.Stream(self.dev)
         self.s_down = [torch.cuda.Stream(self.dev) for _ in range(lanes)]
         self.in_lane = self._deal([h.numel() * h.element_size() for h in self.hin], lanes)
         self.out_lane = self._deal([h.numel() * h.element_size() for h in self.hout], lanes)
@@ -372,7 +371,7 @@ class PipelinedPasses:
             if k >= 2:
                 for e in down[k - 2]:
                     self.s_run.wait_event(e)
-            p.run_overlapped(self.s_run, self.s_side)
+            p.run(self.s_run)
             comp.append(torch.cuda.Event())
             comp[k].record(self.s_run)
             for st in self.s_down:
