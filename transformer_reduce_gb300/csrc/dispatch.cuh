@@ -5,10 +5,9 @@
 // template parameters; the launcher picks the smallest instantiation whose
 // capacity covers the row.  The HW4 page's ITERATIONS buckets for the softmax
 // backward (row lengths 32 ... 2048) all land on register-resident buckets
-// here: 16-bit storage holds up to 2048 elements in one warp for the backward
-// (32 threads x 8 chunks x 8 elements) and 1024 for the pipelined forward
-// (which keeps two rows in registers); longer rows use several warps per row,
-// up to 16384 elements, and the looped path beyond.
+// here: 16-bit storage holds up to 1024 elements in one warp (32 threads x 4
+// chunks x 8 elements), and longer rows use several warps per row, up to
+// 16384 elements, with the looped path beyond.
 #pragma once
 
 #include "launch.h"
@@ -24,8 +23,12 @@ namespace lsr {
 // without spilling.  Longer rows take the looped path.
 constexpr int kSoftmaxFwMaxCpt = 4;  // chunks per thread, softmax forward buckets
 constexpr int kSoftmaxFwMaxTpr = 512;  // 16-bit: 16384 keys per row in registers
-constexpr int kSoftmaxBwMaxCpt = 8;  // chunks per thread, softmax backward buckets
-constexpr int kSoftmaxBwMaxTpr = 256;  // 16-bit: 16384 keys per row in registers
+// The backward holds both y and dout: at most four chunks per thread (80
+// registers), two or more warps per row beyond 128 chunks (2048 keys of
+// 16-bit storage: 32 x 8 took 154 registers, one block per SM, 0.88 of peak;
+// 64 x 4 reaches the copy peak)
+constexpr int kSoftmaxBwMaxCpt = 4;  // chunks per thread, softmax backward buckets
+constexpr int kSoftmaxBwMaxTpr = 512;  // 16-bit: 16384 keys per row in registers
 constexpr int kLnMaxCpt = 4;         // chunks per thread, LayerNorm buckets
 constexpr int kLnMaxTpr = 512;       // 16-bit: 16384 features per row in registers
 constexpr int kLoopWarpRowMax = 2048;  // looped path: one warp per row up to here
@@ -151,7 +154,7 @@ constexpr int kLnDinpStages = 3;
 #define LSR_SOFTMAX_FW_BUCKETS(X) LSR_DENSE4_BUCKETS(X)
 #define LSR_SOFTMAX_BW_BUCKETS(X)                                               \
     X(1, 1) X(2, 1) X(4, 1) X(8, 1) X(16, 1) X(32, 1) X(32, 2) X(32, 3) X(32, 4) \
-    X(32, 5) X(32, 6) X(32, 7) X(32, 8) X(64, 8) X(128, 8) X(256, 8)
+    X(64, 4) X(128, 4) X(256, 4) X(512, 4)
 #define LSR_LN_BUCKETS(X) LSR_DENSE4_BUCKETS(X)
 
 template <typename T>

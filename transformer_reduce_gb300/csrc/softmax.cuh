@@ -506,13 +506,16 @@ __device__ __forceinline__ void keep_elements(uint4 &u, uint32_t bits) {
 // y and dout are cleared to 0 before the arithmetic, so they add nothing to
 // the sum and their output is 0, whatever the memory held there.
 //
-// Resident 256-thread blocks per SM asked of ptxas: four for the two-chunk
-// bucket (64 registers; left alone ptxas keeps the unpacked rows live across
-// the reduction and takes 96, five spill), fewer for wider rows, and 0 (its
-// own heuristic) where a cap would spill.
+// Resident blocks per SM asked of ptxas: four 256-thread blocks for the
+// two-chunk bucket (64 registers; left alone ptxas keeps the unpacked rows
+// live across the reduction and takes 96, five spill), fewer for wider rows,
+// 768 threads per SM for multi-warp rows (85 registers; left alone ptxas
+// takes 127 for 256-thread rows), and 0 (its own heuristic) where a cap
+// would spill.
 template <int TPR, int CPT>
 constexpr int softmax_bw_masked_min_blocks() {
-    return TPR <= 32 ? (CPT <= 1 ? 5 : CPT <= 2 ? 4 : CPT <= 3 ? 3 : CPT <= 6 ? 2 : 0) : 0;
+    return TPR <= 32 ? (CPT <= 1 ? 5 : CPT <= 2 ? 4 : CPT <= 3 ? 3 : CPT <= 6 ? 2 : 0)
+                     : (TPR <= 256 ? 768 / TPR : 0);
 }
 
 template <typename T, int TPR, int CPT>
