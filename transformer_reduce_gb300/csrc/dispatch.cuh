@@ -342,8 +342,9 @@ cudaError_t launch_ln_dgdb(float *dgamma, float *dbeta, const T *dy, const T *x,
 // thread: the per-column accumulators then fit in registers next to the row
 // (one chunk per thread measured slower: more threads and barriers per row).
 #define LSR_FUSED_BW_BUCKETS(X)                                                 \
-    X(1, 1) X(1, 2) X(2, 2) X(4, 2) X(8, 2) X(16, 2) X(32, 2) X(64, 2) X(128, 2) \
-    X(128, 3) X(128, 4) X(256, 2) X(256, 3) X(256, 4) X(512, 3) X(512, 4)
+    X(1, 1) X(1, 2) X(2, 2) X(4, 2) X(8, 2) X(16, 2) X(32, 2) X(32, 3) X(64, 2)  \
+    X(64, 3) X(128, 2) X(128, 3) X(128, 4) X(256, 2) X(256, 3) X(256, 4) X(512, 3) \
+    X(512, 4)
 constexpr int kFusedMaxCpt = 2;
 
 
@@ -356,11 +357,18 @@ cudaError_t launch_ln_bw_fused(T *dx, float *dgamma, float *dbeta, const T *dy, 
     // Chunks per thread: two (the row's g and xhat held for the epilogue) up
     // to 256 vectors; four above (g and xhat unpacked again from the staged
     // row), where 256 threads with four chunks beat 512 with two (8192
-    // features on GB300: 179 -> 143 us).
+    // features on GB300: 179 -> 143 us).  From 64 vectors up, the bucket of
+    // up to four chunks is also taken when it covers the row with fewer idle
+    // slots (768 features: 32 x 3 instead of 64 x 2, 20.8 -> 17.2 us).
     const int64_t nvec = N / V;
-    const bool four = nvec > 256;
-    const bool picked = pick_bucket_dense(nvec, four ? kLnMaxCpt : kFusedMaxCpt, kLnMaxTpr, &tpr,
-                                          &cpt);
+    int tpr2 = 0, cpt2 = 0, tpr4 = 0, cpt4 = 0;
+    const bool ok2 = pick_bucket_dense(nvec, kFusedMaxCpt, kLnMaxTpr, &tpr2, &cpt2);
+    const bool ok4 = pick_bucket_dense(nvec, kLnMaxCpt, kLnMaxTpr, &tpr4, &cpt4);
+    const bool four = nvec > 256 ||
+                      (nvec >= 64 && ok4 && (!ok2 || tpr4 * cpt4 < tpr2 * cpt2));
+    const bool picked = four ? ok4 : ok2;
+    tpr = four ? tpr4 : tpr2;
+    cpt = four ? cpt4 : cpt2;
     if (rows > 0 && vec && picked) {
         int64_t nparts = 0;
         cudaError_t e = cudaErrorInvalidValue;
