@@ -832,3 +832,98 @@ def test_ln_bw_fused_zero_rows_and_workspace_rejection():
     small = torch.empty(need // 4 - 1, device=DEV)
     with pytest.raises(L.LsError):
         L.layernorm_bw(li["dy"], li["x"], li["gamma"], m, m, workspace=small)
+
+
+# ----------------------------------------------------------------------------
+# mask forms: the kernels classify each batch entry's mask row as a window of
+# visible keys or as "general"; every form must give the oracle's result
+# ----------------------------------------------------------------------------
+
+def _mask_forms(B, Tk, dt, seed):
+    """[B, Tk] additive masks cycling through the forms the kernels tell
+    apart: right padding (with -0.0 among the visible keys), left padding, a
+    window in the middle, -inf holes inside the visible keys, finite biases
+    with right padding, nothing visible, and no padding at all."""
+    g = torch.Generator().manual_seed(seed)
+    m = torch.zeros(B, Tk)
+    for b in range(B):
+        form = b % 7
+        lo = int(torch.randint(1, max(2, Tk // 3), (1,), generator=g))
+        hi = int(torch.randint(max(lo + 1, Tk // 2), Tk, (1,), generator=g))
+        if form == 0:
+            m[b, hi:] = -math.inf
+            m[b, 1:hi:5] = -0.0
+        elif form == 1:
+            m[b, :lo] = -math.inf
+        elif form == 2:
+            m[b, :lo] = -math.inf
+            m[b, hi:] = -math.inf
+        elif form == 3:
+            m[b, hi:] = -math.inf
+            m[b, lo:lo + 3] = -math.inf
+        elif form == 4:
+            m[b] = torch.randn(Tk, generator=g)
+            m[b, hi:] = -math.inf
+        elif form == 5:
+            m[b] = -math.inf
+    return m.to(dt).to(DEV)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "f16", "bf16"])
+@pytest.mark.parametrize("H,Tq,Tk,causal", [
+    (2, 16, 256, False), (2, 64, 64, True), (1, 40, 512, True),   # Tq < Tk: bottom-right
+    (2, 8, 1000, False),                                          # ragged chunk count
+    (2, 8, 100, True),                                            # 16-bit: looped path
+])
+def test_softmax_mask_forms(dtype, H, Tq, Tk, causal):
+    """Forward, scaled forward and masked backward (with garbage at invisible
+    keys) on every mask form, each against the oracle."""
+    L = _L()
+    dt = _dt(dtype)
+    B = 14
+    g = torch.Generator(device=DEV).manual_seed(Tk + Tq)
+    x = torch.randn(B, H, Tq, Tk, generator=g, device=DEV).mul(3).to(dt)
+    dout = torch.randn(B, H, Tq, Tk, generator=g, device=DEV).to(dt)
+    mask = _mask_forms(B, Tk, dt, seed=Tk)
+    y = L.softmax_fw(x, mask, causal=causal)
+    ys = L.softmax_fw(x, mask, causal=causal, scale=0.3)
+    torch.cuda.synchronize()
+    ref = oracle.softmax_fw_tensor_offset(x.cpu(), mask.cpu(), causal=causal)
+    compare(y, ref, dtype, f"mask forms fw {Tq}x{Tk}")
+    assert np.all(y.cpu().float().numpy()[ref == 0.0] == 0.0)
+    refs = oracle.softmax_fw_tensor_scaled(x.cpu(), mask.cpu(), causal=causal, scale=0.3)
+    compare(ys, refs, dtype, f"mask forms scaled fw {Tq}x{Tk}")
+    invisible = torch.from_numpy(ref == 0.0).to(DEV)
+    y_in = torch.from_numpy(ref).to(dt).to(DEV)
+    y_dirty = torch.where(invisible, torch.full_like(y_in, 5.0), y_in)
+    d_dirty = torch.where(invisible, torch.full_like(dout, float("nan")), dout)
+    dx = L.softmax_bw_masked(d_dirty, y_dirty, mask, causal=causal)
+    torch.cuda.synchronize()
+    want = oracle.softmax_bw_masked_tensor(torch.nan_to_num(d_dirty, nan=0.0).cpu(),
+                                           y_dirty.cpu(), mask.cpu(), causal=causal)
+    compare(dx, want, dtype, f"mask forms masked bw {Tq}x{Tk}")
+    assert torch.all(dx[invisible] == 0)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("H,Tq", [(1, 1), (1, 2), (2, 3)])
+def test_softmax_many_batch_entries_per_block(dtype, H, Tq):
+    """A block whose rows span more batch entries than it classifies (one or
+    two rows per entry) treats every mask row as general; results as the
+    oracle's for every form."""
+    L = _L()
+    dt = _dt(dtype)
+    B, Tk = 700, 64
+    g = torch.Generator(device=DEV).manual_seed(B + H + Tq)
+    x = torch.randn(B, H, Tq, Tk, generator=g, device=DEV).mul(3).to(dt)
+    dout = torch.randn(B, H, Tq, Tk, generator=g, device=DEV).to(dt)
+    mask = _mask_forms(B, Tk, dt, seed=B + Tq)
+    y = L.softmax_fw(x, mask, causal=False)
+    torch.cuda.synchronize()
+    ref = oracle.softmax_fw_tensor(x.cpu(), mask.cpu())
+    compare(y, ref, dtype, f"many entries fw H={H} Tq={Tq}")
+    y_in = torch.from_numpy(ref).to(dt).to(DEV)
+    dx = L.softmax_bw_masked(dout, y_in, mask)
+    torch.cuda.synchronize()
+    compare(dx, oracle.softmax_bw_masked_tensor(dout.cpu(), y_in.cpu(), mask.cpu()), dtype,
+            f"many entries masked bw H={H} Tq={Tq}")
