@@ -21,8 +21,9 @@ configurations -- softmax [8,16,T,T] bf16 for T in {768, 1024, 2048} and
 LayerNorm [16384, N] bf16 for N in {4096, 8192} -- and on the encoder shapes
 (``large_configs``, ``encoder_cold``); the widened kernels (``next_rows``);
 the same layer with the fused LayerNorm backward and the masked softmax
-backward (``fused_pass``); and the end-to-end pass fed from pinned host
-memory (``e2e``).
+backward (``fused_pass``); the pass replayed from a CUDA graph
+(``graph_pass``); and the end-to-end pass fed from pinned host memory
+(``e2e``).
 
 --impl reference times the CPU oracle (fp64 C, on all host cores) on a
 bounded row sample of the same workload; it is a deliberately slow baseline.
@@ -494,6 +495,37 @@ def run_ours(args):
                 "softmax backward is done (when its dy would exist)"}
     floor_us = event_floor_us(stream, dev)
 
+    # the same one-stream pass captured in a CUDA graph (ten passes per graph,
+    # the library calls recorded once and replayed): the launch boundaries
+    # cost less when the GPU front end replays a graph
+    graph_pass = None
+    if not args.no_graph:
+        g = torch.cuda.CUDAGraph()
+        per_graph = 10
+        torch.cuda.synchronize(dev)
+        with torch.cuda.graph(g, stream=stream):
+            for _ in range(per_graph):
+                path.run(stream)
+        torch.cuda.synchronize(dev)
+        for _ in range(max(1, args.warmup // per_graph + 1)):
+            g.replay()
+        reps = max(args.steps // per_graph, int(min_s / (pass_s * per_graph)) + 1)
+        cs = torch.cuda.current_stream(dev)
+        g0 = torch.cuda.Event(enable_timing=True)
+        g1 = torch.cuda.Event(enable_timing=True)
+        g0.record(cs)
+        for _ in range(reps):
+            g.replay()
+        g1.record(cs)
+        torch.cuda.synchronize(dev)
+        graph_s = max_over_ranks(g0.elapsed_time(g1) / 1e3, world)
+        graph_pass = {
+            "steps": reps * per_graph, "passes_per_graph": per_graph,
+            "ms_per_step": round(graph_s / (reps * per_graph) * 1e3, 5),
+            "gbs": round(sum_over_ranks(step_bytes * reps * per_graph, world) / graph_s / 1e9, 1),
+            "note": "the headline's calls captured once in a CUDA graph and replayed"}
+        del g
+
     # the same layer with the fused LayerNorm backward and the masked softmax
     # backward, one stream, at least min_s of passes
     fused_bytes = path.fused_step_bytes()
@@ -591,6 +623,7 @@ def run_ours(args):
                 "gbs": round(world * path.dense_step_bytes() * args.steps / job_s / 1e9, 1),
                 "note": "as if the softmax forward read masked keys too"},
             "overlapped": overlapped,
+            "graph_pass": graph_pass,
             "kernels": kernels,
             "kernels_note": (f"in-pass, one stream, {kernel_steps} passes, a CUDA event pair "
                              f"around every call; such a pair around a call that does almost "
@@ -680,6 +713,8 @@ def main(argv=None):
                          "cold-L2 measurement")
     ap.add_argument("--no-cold", action="store_true",
                     help="skip the cold-L2 single-kernel tables")
+    ap.add_argument("--no-graph", action="store_true",
+                    help="skip the CUDA-graph replay of the pass")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
