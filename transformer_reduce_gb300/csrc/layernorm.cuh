@@ -53,9 +53,9 @@ constexpr size_t ln_smem() {
 //
 // Each row group owns a contiguous range of rows.  Rows are staged into
 // shared memory S-1 rows ahead with per-thread cp.async copies (each thread
-// reads back only its own chunks), so the loads of several rows are in
-// flight while one is reduced.  A thread's columns are the same for every
-// row: its gamma/beta chunks are loaded once.
+// reads back only its own chunks), so the loads of the next rows are in
+// flight while one is reduced (the launcher takes S = 2).  A thread's columns
+// are the same for every row: its gamma/beta chunks are loaded once.
 // ----------------------------------------------------------------------------
 // RMS = true is RMSNorm (the FastTransformer page, section 5.4): no shift and
 // no mean, one sum of squares, y = x * rstd * gamma; `mean` and `beta` are
