@@ -138,14 +138,19 @@ cudaError_t launch_persistent(int block, size_t smem, int64_t work_blocks, cudaS
 }
 
 // Stages of the cp.async row pipelines (rows in flight per row group = S - 1).
-// The LayerNorm kernels keep one row in flight: their occupancy is bound by
-// registers either way, and the smaller ring measured faster at every width
-// but 2048 (GB300, bf16, 16384 rows: forward 13.5 -> 12.5 us at 1024
-// features, 86.7 -> 84.1 us at 8192; input gradient 122.3 -> 117.5 us at
-// 8192; fused backward 75.2 -> 71.9 us at 4096).
+// LayerNorm: rows of up to 4 KB keep three (forward) or two (input gradient)
+// rows in flight -- inside a layer's pass, where they often find their input
+// warm in L2, that measured about 1 us per encoder pass faster -- and wider,
+// HBM-bound rows keep one, which measured 3-5 % faster there (GB300, bf16,
+// 16384 rows: forward 90.7 -> 87.5 us at 8192 features, input gradient
+// 126.2 -> 119.7 us).  The fused backward keeps one at every width (75.2 ->
+// 71.9 us at 4096 features).
 constexpr int kSoftmaxFwStages = 4;
-constexpr int kLnFwStages = 2;
-constexpr int kLnDinpStages = 2;
+template <int TPR, int CPT>
+constexpr int ln_fw_stages() { return TPR * CPT * 16 <= 4096 ? 4 : 2; }
+template <int TPR, int CPT>
+constexpr int ln_dinp_stages() { return TPR * CPT * 16 <= 4096 ? 3 : 2; }
+constexpr int kLnBwFusedStages = 2;
 
 // ----------------------------------------------------------------------------
 // softmax
@@ -251,8 +256,8 @@ cudaError_t launch_norm_fw(T *y, float *mean, float *rstd, const T *x, const T *
     if (vec && pick_bucket_dense(N / V, kLnMaxCpt, kLnMaxTpr, &tpr, &cpt)) {
 #define X(TPR_, CPT_)                                                                     \
     if (tpr == TPR_ && cpt == CPT_)                                                       \
-        return launch_persistent<ln_fw_vec<T, TPR_, CPT_, kLnFwStages, RMS>>(                  \
-            block_threads<TPR_>(), ln_smem<TPR_, CPT_, kLnFwStages, 1, 1>(),                \
+        return launch_persistent<ln_fw_vec<T, TPR_, CPT_, ln_fw_stages<TPR_, CPT_>(), RMS>>(  \
+            block_threads<TPR_>(), ln_smem<TPR_, CPT_, ln_fw_stages<TPR_, CPT_>(), 1, 1>(),   \
             ceil_div(rows, rows_per_block<TPR_>()), st, y, mean, rstd, x, gamma, beta, rows,  \
             (int)N, eps);
         LSR_LN_BUCKETS(X)
@@ -287,8 +292,8 @@ cudaError_t launch_norm_dinp(T *dx, const T *dy, const T *x, const T *gamma,
     if (vec && pick_bucket_dense(N / V, kLnMaxCpt, kLnMaxTpr, &tpr, &cpt)) {
 #define X(TPR_, CPT_)                                                                       \
     if (tpr == TPR_ && cpt == CPT_)                                                         \
-        return launch_persistent<ln_dinp_vec<T, TPR_, CPT_, kLnDinpStages, RMS>>(                \
-            block_threads<TPR_>(), ln_smem<TPR_, CPT_, kLnDinpStages, 2, 2>(),                \
+        return launch_persistent<ln_dinp_vec<T, TPR_, CPT_, ln_dinp_stages<TPR_, CPT_>(), RMS>>( \
+            block_threads<TPR_>(), ln_smem<TPR_, CPT_, ln_dinp_stages<TPR_, CPT_>(), 2, 2>(),  \
             ceil_div(rows, rows_per_block<TPR_>()), st, dx, dy, x, gamma, mean, rstd, rows,     \
             (int)N);
         LSR_LN_BUCKETS(X)
@@ -325,10 +330,23 @@ cudaError_t launch_ln_dgdb(float *dgamma, float *dbeta, const T *dy, const T *x,
         if (vec) {
             constexpr int V = Traits<T>::kVec;
             dim3 grid((unsigned)ceil_div(N, 32 * V), (unsigned)nchunks);
-            constexpr size_t smem = ln_dgdb_staged_smem<T>();
-            ensure_dynamic_smem<ln_dgdb_staged<T>>(smem);
-            cudaError_t e = launch_pdl(ln_dgdb_staged<T>, grid, dim3(kDgdbWarps * 32), smem, st,
-                                       part, dy, x, mean, rstd, rows, N, rpc);
+            // Ring depth: four stages (six rows in flight per warp) for rows of
+            // up to 4 KB, which inside a layer's backward usually follow the
+            // input gradient's read of the same dy and x (warm in L2; the
+            // encoder pass measured 1.7 us faster than with two); two stages
+            // for wider rows (cold, HBM-bound: 2-4 % faster than four).
+            cudaError_t e;
+            if (N * (int64_t)sizeof(T) <= 4096) {
+                constexpr size_t smem = ln_dgdb_staged_smem<4>();
+                ensure_dynamic_smem<ln_dgdb_staged<T, 4>>(smem);
+                e = launch_pdl(ln_dgdb_staged<T, 4>, grid, dim3(kDgdbWarps * 32), smem, st, part,
+                               dy, x, mean, rstd, rows, N, rpc);
+            } else {
+                constexpr size_t smem = ln_dgdb_staged_smem<2>();
+                ensure_dynamic_smem<ln_dgdb_staged<T, 2>>(smem);
+                e = launch_pdl(ln_dgdb_staged<T, 2>, grid, dim3(kDgdbWarps * 32), smem, st, part,
+                               dy, x, mean, rstd, rows, N, rpc);
+            }
             if (e != cudaSuccess) return e;
         } else {
             dim3 grid((unsigned)ceil_div(N, 32), (unsigned)nchunks);
@@ -381,9 +399,9 @@ cudaError_t launch_ln_bw_fused(T *dx, float *dgamma, float *dbeta, const T *dy, 
     if (tpr == TPR_ && cpt == CPT_) {                                                       \
         const int64_t rpc = ceil_div(rows, (int64_t)ln_bw_fused_chunks<TPR_, CPT_>());      \
         nparts = ceil_div(rows, rpc);                                                       \
-        constexpr size_t smem = ln_bw_fused_smem<TPR_, CPT_, kLnDinpStages, V>();            \
-        ensure_dynamic_smem<ln_bw_fused_vec<T, TPR_, CPT_, kLnDinpStages>>(smem);            \
-        e = launch_pdl(ln_bw_fused_vec<T, TPR_, CPT_, kLnDinpStages>,                        \
+        constexpr size_t smem = ln_bw_fused_smem<TPR_, CPT_, kLnBwFusedStages, V>();            \
+        ensure_dynamic_smem<ln_bw_fused_vec<T, TPR_, CPT_, kLnBwFusedStages>>(smem);            \
+        e = launch_pdl(ln_bw_fused_vec<T, TPR_, CPT_, kLnBwFusedStages>,                        \
                        dim3((unsigned)nparts),                                               \
                        dim3(ln_bw_fused_block<TPR_>()), smem, st, dx, part, dy, x, gamma,    \
                        mean, rstd, rows, (int)N, rpc);                                       \

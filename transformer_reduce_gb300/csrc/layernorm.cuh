@@ -54,8 +54,9 @@ constexpr size_t ln_smem() {
 // Each row group owns a contiguous range of rows.  Rows are staged into
 // shared memory S-1 rows ahead with per-thread cp.async copies (each thread
 // reads back only its own chunks), so the loads of the next rows are in
-// flight while one is reduced (the launcher takes S = 2).  A thread's columns
-// are the same for every row: its gamma/beta chunks are loaded once.
+// flight while one is reduced (the launcher picks S by the row's width).  A
+// thread's columns are the same for every row: its gamma/beta chunks are
+// loaded once.
 // ----------------------------------------------------------------------------
 // RMS = true is RMSNorm (the FastTransformer page, section 5.4): no shift and
 // no mean, one sum of squares, y = x * rstd * gamma; `mean` and `beta` are
@@ -696,21 +697,22 @@ ln_dgdb_partial(float *part, const T *dy, const T *x, const float *mean,
 // ln_dgdb_partial over tiles of 32 lanes x 16 bytes (256 columns of 16-bit
 // storage), with the same warp-to-row assignment, fp32 arithmetic and
 // warp-order combine; each warp streams its rows through a private ring of
-// kDgdbStages cp.async stages of kDgdbRows rows each (512 contiguous bytes of
-// dy and of x per row, plus the rows' mean and rstd), so that
-// (kDgdbStages - 1) * kDgdbRows rows per warp are in flight and the per-stage
-// bookkeeping is shared by kDgdbRows rows.  The ring is reused for the
-// warp-order combine at the end.  mean == nullptr means mean 0 (RMSNorm).
+// S cp.async stages of kDgdbRows rows each (512 contiguous bytes of dy and of
+// x per row, plus the rows' mean and rstd), so that (S - 1) * kDgdbRows rows
+// per warp are in flight and the per-stage bookkeeping is shared by
+// kDgdbRows rows.  The ring is reused for the warp-order combine at the end.
+// The ring depth does not change which rows a warp adds or in what order, so
+// the result is the same bit for bit whichever depth the launcher takes.
+// mean == nullptr means mean 0 (RMSNorm).
 // ----------------------------------------------------------------------------
-constexpr int kDgdbStages = 4;
 constexpr int kDgdbRows = 2;
 
-template <typename T>
+template <int S>
 constexpr size_t ln_dgdb_staged_smem() {
-    return (size_t)kDgdbWarps * kDgdbStages * kDgdbRows * (64 * 16 + 2 * 4);
+    return (size_t)kDgdbWarps * S * kDgdbRows * (64 * 16 + 2 * 4);
 }
 
-template <typename T>
+template <typename T, int S>
 __global__ void __launch_bounds__(kDgdbWarps * 32, 3)
 ln_dgdb_staged(float *part, const T *dy, const T *x, const float *mean, const float *rstd,
                int64_t rows, int64_t N, int64_t rows_per_chunk) {
@@ -718,7 +720,6 @@ ln_dgdb_staged(float *part, const T *dy, const T *x, const float *mean, const fl
     using Tr = Traits<T>;
     constexpr int V = Tr::kVec;
     constexpr int CT = 32 * V;  // columns per tile
-    constexpr int S = kDgdbStages;
     constexpr int R = kDgdbRows;
     static_assert(2 * kDgdbWarps * CT * 4 <= kDgdbWarps * S * R * 64 * 16, "combine fits the ring");
     extern __shared__ uint4 dsmem[];
