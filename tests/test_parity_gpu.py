@@ -224,6 +224,30 @@ def test_overlapped_pass_matches_the_serial_pass():
         assert torch.equal(x, y)
 
 
+def test_pass_replayed_from_a_cuda_graph_matches_the_eager_pass():
+    """The library's calls can be captured in a CUDA graph (they allocate and
+    synchronise nothing); the replay writes exactly the eager pass's outputs."""
+    from transformer_reduce_gb300 import workloads as W
+    from transformer_reduce_gb300.layer_path import LayerReducePath
+    mk = lambda: LayerReducePath(W.GPT2_SMALL["softmax"],  # noqa: E731
+                                 [W.GPT2_SMALL["layernorm"], W.TINY["layernorm"]], device=DEV)
+    a, b = mk(), mk()
+    st = torch.cuda.Stream()
+    a.run(st)
+    b.run(st)  # first calls (occupancy queries, attributes) outside the capture
+    torch.cuda.synchronize()
+    for t in b._outputs():
+        t.fill_(float("nan"))
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=st):
+        b.run(st)
+    g.replay()
+    g.replay()
+    torch.cuda.synchronize()
+    for x, y in zip(a._outputs(), b._outputs()):
+        assert torch.equal(x, y)
+
+
 def test_fused_pass_matches_the_serial_pass():
     """The layer with the fused LayerNorm backward and the masked softmax
     backward (the benchmark's fused_pass) gives the outputs of the plain pass
