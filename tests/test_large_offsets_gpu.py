@@ -68,7 +68,7 @@ def test_softmax_past_2_pow_32_elements(lib):
     rows = sample_rows(rows_n, boundaries=edges, k=128, seed=103)
     assert rows.max() * T >= (1 << 32)
     compare(take_rows(y, rows), oracle_softmax_rows(x, mask, rows, False), "bf16",
-            "softmax fw past 2^32 elements")
+            "past-2^32 softmax_fw")
     del x, y
     torch.cuda.empty_cache()
 
@@ -79,12 +79,12 @@ def test_softmax_past_2_pow_32_elements(lib):
     dx = L.softmax_bw(dout, yin)
     torch.cuda.synchronize()
     compare(take_rows(dx, rows), oracle.softmax_bw(take_rows(dout, rows), take_rows(yin, rows)),
-            "bf16", "softmax bw past 2^32 elements")
+            "bf16", "past-2^32 softmax_bw")
     L.softmax_bw_masked(dout, yin, mask, dinp=dx)
     torch.cuda.synchronize()
     want = oracle.softmax_bw_masked(take_rows(dout, rows), take_rows(yin, rows), mask.cpu(),
                                     batch=rows // (H * T))
-    compare(take_rows(dx, rows), want, "bf16", "masked softmax bw past 2^32 elements")
+    compare(take_rows(dx, rows), want, "bf16", "past-2^32 masked bw")
 
 
 def test_softmax_past_2_pow_31_rows(lib):
@@ -102,7 +102,7 @@ def test_softmax_past_2_pow_31_rows(lib):
     rows = sample_rows(Tq, boundaries=[(1 << 31) - 1, 1 << 31], k=64, seed=112)
     assert rows.max() > (1 << 31)
     compare(take_rows(y, rows), oracle_softmax_rows(x, mask, rows, False), "bf16",
-            "softmax fw past 2^31 rows")
+            "past-2^31-rows softmax_fw")
     del x, y
     torch.cuda.empty_cache()
 
@@ -113,11 +113,11 @@ def test_softmax_past_2_pow_31_rows(lib):
     torch.cuda.synchronize()
     want = oracle.softmax_bw_masked(take_rows(dout, rows), take_rows(yin, rows), mask.cpu(),
                                     batch=np.zeros_like(rows))
-    compare(take_rows(dx, rows), want, "bf16", "masked softmax bw past 2^31 rows")
+    compare(take_rows(dx, rows), want, "bf16", "past-2^31-rows masked bw")
     L.softmax_bw(dout, yin, dinp=dx)
     torch.cuda.synchronize()
     compare(take_rows(dx, rows), oracle.softmax_bw(take_rows(dout, rows), take_rows(yin, rows)),
-            "bf16", "softmax bw past 2^31 rows")
+            "bf16", "past-2^31-rows softmax_bw")
 
 
 def test_layernorm_past_2_pow_32_elements(lib):
@@ -140,9 +140,9 @@ def test_layernorm_past_2_pow_32_elements(lib):
     rows = sample_rows(R, boundaries=[(1 << 31) // N, (1 << 32) // N], k=128, seed=122)
     assert rows.max() * N >= (1 << 32)
     yr, mr, rr = oracle.layernorm_fw(take_rows(x, rows), gamma.cpu(), beta.cpu(), eps)
-    compare(take_rows(y, rows), yr, "bf16", "ln fw y past 2^32 elements")
-    compare(mean.cpu()[rows], mr, "bf16", "ln fw mean past 2^32 elements")
-    compare(rstd.cpu()[rows], rr, "bf16", "ln fw rstd past 2^32 elements")
+    compare(take_rows(y, rows), yr, "bf16", "past-2^32 ln_fw y")
+    compare(mean.cpu()[rows], mr, "bf16", "past-2^32 ln_fw mean")
+    compare(rstd.cpu()[rows], rr, "bf16", "past-2^32 ln_fw rstd")
     del y, mean, rstd
     torch.cuda.empty_cache()
 
@@ -162,13 +162,13 @@ def test_layernorm_past_2_pow_32_elements(lib):
     dx = L.layernorm_bw_dinp(dy, x, gamma, mean_in, rstd_in)
     dgm, dbt = L.layernorm_bw_dgamma_dbeta(dy, x, mean_in, rstd_in)
     torch.cuda.synchronize()
-    compare(take_rows(dx, rows), want_dx, "bf16", "ln dinp past 2^32 elements")
-    compare(dgm.cpu()[cols], want_g, "bf16", "ln dgamma over 2^22 rows")
-    compare(dbt.cpu()[cols], want_b, "bf16", "ln dbeta over 2^22 rows")
+    compare(take_rows(dx, rows), want_dx, "bf16", "past-2^32 ln_dinp")
+    compare(dgm.cpu()[cols], want_g, "bf16", "past-2^32 ln_dgamma")
+    compare(dbt.cpu()[cols], want_b, "bf16", "past-2^32 ln_dbeta")
 
     dx.zero_()
     dx, dgm, dbt = L.layernorm_bw(dy, x, gamma, mean_in, rstd_in, dx=dx)
     torch.cuda.synchronize()
-    compare(take_rows(dx, rows), want_dx, "bf16", "fused ln bw dx past 2^32 elements")
-    compare(dgm.cpu()[cols], want_g, "bf16", "fused ln bw dgamma over 2^22 rows")
-    compare(dbt.cpu()[cols], want_b, "bf16", "fused ln bw dbeta over 2^22 rows")
+    compare(take_rows(dx, rows), want_dx, "bf16", "past-2^32 fused ln bw dx")
+    compare(dgm.cpu()[cols], want_g, "bf16", "past-2^32 fused ln bw dgamma")
+    compare(dbt.cpu()[cols], want_b, "bf16", "past-2^32 fused ln bw dbeta")

@@ -101,13 +101,15 @@ cudaError_t launch_pdl(void (*k)(KArgs...), dim3 grid, dim3 block, size_t smem, 
 }
 
 // Resident blocks per SM of one kernel instantiation with `smem` bytes of
-// dynamic shared memory (queried once; the opt-in above 48 KB is set once per
-// device before the first launch there).
+// dynamic shared memory (queried once).  The opt-in to more than 48 KB per
+// block is set once per device before the first launch there, for any
+// dynamic size: the 48 KB default counts the kernel's static shared memory
+// too, so a dynamic size just under it can already need the opt-in.
 template <auto K>
 void ensure_dynamic_smem(size_t smem) {
     static std::atomic<int> configured[kMaxDevices];
     int dev = 0;
-    if (smem > 48 * 1024 && cudaGetDevice(&dev) == cudaSuccess && dev >= 0 &&
+    if (smem > 0 && cudaGetDevice(&dev) == cudaSuccess && dev >= 0 &&
         dev < kMaxDevices && !configured[dev].load(std::memory_order_acquire)) {
         cudaFuncSetAttribute(K, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         configured[dev].store(1, std::memory_order_release);

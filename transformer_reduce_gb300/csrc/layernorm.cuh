@@ -304,7 +304,10 @@ ln_dinp_vec(T *dx, const T *dy, const T *x, const T *gamma, const float *mean,
 // Fused backward: dx, and the dgamma / dbeta partial sums of one row chunk,
 // from one read of dy and x.  Block b owns rows [b*rpc, (b+1)*rpc) (a fixed
 // cut of the rows, independent of the GPU); its G row groups split them into
-// contiguous runs and go through the same staged pipeline as ln_dinp_vec.
+// contiguous runs and stage dy and x as ln_dinp_vec does, while each thread
+// reads the row's mean and rstd into registers one row ahead (with a
+// per-thread 4-byte cp.async of them into the stage, as the input gradient
+// stages them, this kernel took 11-30 % longer at 768-2048 features).
 // Each thread also accumulates dgamma += dy * xhat and dbeta += dy for its
 // columns; the G groups' sums are added in group order through shared memory
 // and written as the chunk's partial part[(b*2 + {0,1}) * N + col], which
@@ -336,7 +339,7 @@ template <int TPR, int CPT, int S, int V>
 constexpr size_t ln_bw_fused_smem() {
     // the stage ring, reused at the end for the [G][2][TPR*CPT*V] group sums
     constexpr int BLOCK = ln_bw_fused_block<TPR>();
-    constexpr size_t ring = (size_t)S * BLOCK * (2 * CPT * 16 + 2 * 4);
+    constexpr size_t ring = (size_t)S * BLOCK * 2 * CPT * 16;
     constexpr size_t sums = (size_t)BLOCK * 2 * CPT * V * 4;
     return ring > sums ? ring : sums;
 }
@@ -362,8 +365,7 @@ ln_bw_fused_vec(T *dx, float *part, const T *dy, const T *x, const T *gamma, con
     constexpr int G = BLOCK / TPR;
     constexpr int W = TPR * CPT * V;  // columns a row group covers (>= N)
     extern __shared__ uint4 dsmem[];
-    uint4 *stage = dsmem;                                                    // [S][2][CPT][BLOCK]
-    float *stat = reinterpret_cast<float *>(dsmem + S * 2 * CPT * BLOCK);    // [S][2][BLOCK]
+    uint4 *stage = dsmem;  // [S][2][CPT][BLOCK]
     __shared__ float red[TPR > 32 ? 64 : 1];  // >= 2 * BLOCK / 32 and group_sum2's 48
 
     const int tid = threadIdx.x;
@@ -398,8 +400,6 @@ ln_bw_fused_vec(T *dx, float *part, const T *dy, const T *x, const T *gamma, con
                     cp_async16(&stage[((s * 2 + 1) * CPT + k) * BLOCK + tid], x + off + c * V);
                 }
             }
-            cp_async4(&stat[(s * 2 + 0) * BLOCK + tid], mean + inext);
-            cp_async4(&stat[(s * 2 + 1) * BLOCK + tid], rstd + inext);
         }
         ++inext;
         cp_async_commit();
@@ -407,16 +407,30 @@ ln_bw_fused_vec(T *dx, float *part, const T *dy, const T *x, const T *gamma, con
 #pragma unroll
     for (int s = 0; s < S - 1; ++s) issue(s);
 
+    // the current row's statistics; the next row's are loaded while this
+    // row's data lands and is reduced
+    float mu_c = 0.f, rs_c = 0.f;
+    if (rbeg < rend) {
+        mu_c = __ldg(mean + rbeg);
+        rs_c = __ldg(rstd + rbeg);
+    }
     int s_cur = 0, s_iss = S - 1;
     for (int64_t k = 0; k < per; ++k) {
         issue(s_iss);
         s_iss = s_iss + 1 == S ? 0 : s_iss + 1;
+        const int64_t row = rbeg + k;
+        float mu_n = 0.f, rs_n = 0.f;
+        if (row + 1 < rend) {
+            mu_n = __ldg(mean + row + 1);
+            rs_n = __ldg(rstd + row + 1);
+        }
         cp_async_wait<S - 1>();
 
-        const int64_t row = rbeg + k;
         const bool valid = row < rend;
-        const float mu = valid ? stat[(s_cur * 2 + 0) * BLOCK + tid] : 0.f;
-        const float rs = valid ? stat[(s_cur * 2 + 1) * BLOCK + tid] : 0.f;
+        const float mu = valid ? mu_c : 0.f;
+        const float rs = valid ? rs_c : 0.f;
+        mu_c = mu_n;
+        rs_c = rs_n;
         // Up to two chunks per thread the row's g and xhat stay in registers
         // for the epilogue; wider buckets (whose column accumulators already
         // take 64 registers) unpack them again from the stage instead.
