@@ -58,8 +58,8 @@ constexpr size_t ln_smem() {
 // thread's columns are the same for every row: its gamma/beta chunks are
 // loaded once.  x0 reaches a row's threads by a shuffle from the first
 // lane's staged chunk when the row fits one warp (a per-thread 4-byte copy of
-// it cost the encoder-width forward 5 %), and by a per-thread 4-byte copy for
-// multi-warp rows.
+// it cost the encoder-width forward 5 %); in a multi-warp row each warp's
+// first lane stages it with a 4-byte copy and shuffles it to its warp.
 // ----------------------------------------------------------------------------
 // RMS = true is RMSNorm (the FastTransformer page, section 5.4): no shift and
 // no mean, one sum of squares, y = x * rstd * gamma; `mean` and `beta` are
@@ -107,9 +107,12 @@ ln_fw_vec(T *y, float *mean, float *rstd, const T *x, const T *gamma,
                 const int c = k * TPR + lane;
                 if (c < nchunk) cp_async16(&stage[(s * CPT + k) * BLOCK + tid], xrow + c * V);
             }
-            // the shift: staged per thread for multi-warp rows; a row inside
-            // one warp takes it from its first lane's chunk by a shuffle
-            if constexpr (!RMS && TPR > 32) cp_async4(&x0b[s * BLOCK + tid], xrow);
+            // the shift: a row inside one warp takes it from its first
+            // lane's staged chunk by a shuffle; for a multi-warp row each
+            // warp's first lane stages it and shuffles it to the warp
+            if constexpr (!RMS && TPR > 32) {
+                if ((tid & 31) == 0) cp_async4(&x0b[s * BLOCK + tid], xrow);
+            }
         }
         ++inext;
         cp_async_commit();
@@ -128,7 +131,9 @@ ln_fw_vec(T *y, float *mean, float *rstd, const T *x, const T *gamma,
         float x0 = 0.f;
         if constexpr (!RMS) {
             if constexpr (TPR > 32) {
-                x0 = valid ? first_elem<T>(x0b[s_cur * BLOCK + tid]) : 0.f;
+                const float f =
+                    (valid && (tid & 31) == 0) ? first_elem<T>(x0b[s_cur * BLOCK + tid]) : 0.f;
+                x0 = __shfl_sync(0xffffffffu, f, 0);
             } else {
                 const float f =
                     (valid && lane == 0) ? first_elem<T>(stage[s_cur * CPT * BLOCK + tid].x) : 0.f;
@@ -199,8 +204,8 @@ ln_fw_vec(T *y, float *mean, float *rstd, const T *x, const T *gamma,
 // Input gradient.  g = gamma * dy, xhat = (x - mean)*rstd; S1 = sum g and
 // S2 = sum g*xhat in one fused reduction; then dx = rstd*(g - S1/N - xhat*S2/N).
 // Same staging as the forward: dy and x per stage, and the row's mean / rstd
-// staged by the group's first lane and shuffled to the row's threads (per
-// thread for multi-warp rows; a 4-byte copy by every thread cost 8-16 % at
+// staged by the group's (or, for a multi-warp row, each warp's) first lane
+// and shuffled to its threads (a 4-byte copy by every thread cost 8-16 % at
 // 768-1024 features).
 // ----------------------------------------------------------------------------
 // RMS = true is the RMSNorm input gradient: xhat = x * rstd, one sum
@@ -248,9 +253,10 @@ ln_dinp_vec(T *dx, const T *dy, const T *x, const T *gamma, const float *mean,
                     cp_async16(&stage[((s * 2 + 1) * CPT + k) * BLOCK + tid], x + off + c * V);
                 }
             }
-            // the row's statistics: staged per thread for multi-warp rows, by
-            // the group's first lane (then shuffled) for a row inside one warp
-            if (TPR > 32 || lane == 0) {
+            // the row's statistics: staged by the group's first lane for a
+            // row inside one warp, by each warp's first lane for a multi-warp
+            // row, then shuffled
+            if ((TPR > 32 ? (tid & 31) : lane) == 0) {
                 if constexpr (!RMS) cp_async4(&stat[(s * 2 + 0) * BLOCK + tid], mean + inext);
                 cp_async4(&stat[(s * 2 + 1) * BLOCK + tid], rstd + inext);
             }
@@ -271,8 +277,11 @@ ln_dinp_vec(T *dx, const T *dy, const T *x, const T *gamma, const float *mean,
         const bool valid = row < rend;
         float mu = 0.f, rs = 0.f;
         if constexpr (TPR > 32) {
-            mu = (valid && !RMS) ? stat[(s_cur * 2 + 0) * BLOCK + tid] : 0.f;
-            rs = valid ? stat[(s_cur * 2 + 1) * BLOCK + tid] : 0.f;
+            const bool mine = valid && (tid & 31) == 0;
+            const float m0 = (mine && !RMS) ? stat[(s_cur * 2 + 0) * BLOCK + tid] : 0.f;
+            const float r0 = mine ? stat[(s_cur * 2 + 1) * BLOCK + tid] : 0.f;
+            mu = __shfl_sync(0xffffffffu, m0, 0);
+            rs = __shfl_sync(0xffffffffu, r0, 0);
         } else {
             const bool mine = valid && lane == 0;
             const float m0 = (mine && !RMS) ? stat[(s_cur * 2 + 0) * BLOCK + tid] : 0.f;
