@@ -220,6 +220,7 @@ ln_dinp_vec(T *dx, const T *dy, const T *x, const T *gamma, const float *mean,
     constexpr int H2 = V / 2;
     constexpr int BLOCK = TPR <= 32 ? 256 : TPR;
     constexpr int G = BLOCK / TPR;
+    constexpr int SW = TPR < 32 ? TPR : 32;  // threads sharing one staged copy of the scalars
     extern __shared__ uint4 dsmem[];
     uint4 *stage = dsmem;                                                    // [S][2][CPT][BLOCK]
     float *stat = reinterpret_cast<float *>(dsmem + S * 2 * CPT * BLOCK);    // [S][2][BLOCK]
@@ -253,10 +254,10 @@ ln_dinp_vec(T *dx, const T *dy, const T *x, const T *gamma, const float *mean,
                     cp_async16(&stage[((s * 2 + 1) * CPT + k) * BLOCK + tid], x + off + c * V);
                 }
             }
-            // the row's statistics: staged by the group's first lane for a
-            // row inside one warp, by each warp's first lane for a multi-warp
-            // row, then shuffled
-            if ((TPR > 32 ? (tid & 31) : lane) == 0) {
+            // the row's statistics: staged by the first lane of each slice of
+            // SW threads (the row group, or one warp of a multi-warp row),
+            // then shuffled to the slice
+            if (tid % SW == 0) {
                 if constexpr (!RMS) cp_async4(&stat[(s * 2 + 0) * BLOCK + tid], mean + inext);
                 cp_async4(&stat[(s * 2 + 1) * BLOCK + tid], rstd + inext);
             }
@@ -275,20 +276,11 @@ ln_dinp_vec(T *dx, const T *dy, const T *x, const T *gamma, const float *mean,
 
         const int64_t row = rbeg + k;
         const bool valid = row < rend;
-        float mu = 0.f, rs = 0.f;
-        if constexpr (TPR > 32) {
-            const bool mine = valid && (tid & 31) == 0;
-            const float m0 = (mine && !RMS) ? stat[(s_cur * 2 + 0) * BLOCK + tid] : 0.f;
-            const float r0 = mine ? stat[(s_cur * 2 + 1) * BLOCK + tid] : 0.f;
-            mu = __shfl_sync(0xffffffffu, m0, 0);
-            rs = __shfl_sync(0xffffffffu, r0, 0);
-        } else {
-            const bool mine = valid && lane == 0;
-            const float m0 = (mine && !RMS) ? stat[(s_cur * 2 + 0) * BLOCK + tid] : 0.f;
-            const float r0 = mine ? stat[(s_cur * 2 + 1) * BLOCK + tid] : 0.f;
-            mu = __shfl_sync(0xffffffffu, m0, 0, TPR);
-            rs = __shfl_sync(0xffffffffu, r0, 0, TPR);
-        }
+        const bool mine = valid && tid % SW == 0;
+        const float m0 = (mine && !RMS) ? stat[(s_cur * 2 + 0) * BLOCK + tid] : 0.f;
+        const float r0 = mine ? stat[(s_cur * 2 + 1) * BLOCK + tid] : 0.f;
+        const float mu = __shfl_sync(0xffffffffu, m0, 0, SW);
+        const float rs = __shfl_sync(0xffffffffu, r0, 0, SW);
         float2 g[CPT][H2], xh[CPT][H2];
         float2 s1 = f2(0.f), s2 = f2(0.f);
 #pragma unroll
