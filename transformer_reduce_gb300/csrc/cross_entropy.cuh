@@ -185,6 +185,33 @@ __device__ __forceinline__ float ce_grad(float zj, float l2, float g, bool is_t)
     return g * (is_t ? p - 1.f : p);
 }
 
+// The same for one 16-byte vector, on FP32 pairs; `rel` is the target's index
+// relative to the vector's first element (the target is in this vector when
+// 0 <= rel < kVec, tested once per vector instead of once per logit).  Each
+// element is rounded exactly as ce_grad rounds it.
+template <typename T>
+__device__ __forceinline__ uint4 ce_grad_vec(const uint4 &raw, float l2, float g, int64_t rel) {
+    constexpr int H2 = Traits<T>::kVec / 2;
+    float2 p[H2];
+    unpack2<T>(raw, p);
+#pragma unroll
+    for (int h = 0; h < H2; ++h) {
+        p[h] = fma2(p[h], f2(kLog2e), f2(-l2));
+        p[h].x = fast_exp2(p[h].x);
+        p[h].y = fast_exp2(p[h].y);
+    }
+    if ((uint64_t)rel < (uint64_t)Traits<T>::kVec) {
+#pragma unroll
+        for (int h = 0; h < H2; ++h) {
+            if (rel == 2 * h) p[h].x -= 1.f;
+            if (rel == 2 * h + 1) p[h].y -= 1.f;
+        }
+    }
+#pragma unroll
+    for (int h = 0; h < H2; ++h) p[h] = mul2(f2(g), p[h]);
+    return pack2<T>(p);
+}
+
 // Ignored rows are written as zeros and rows with t >= V as NaN; neither is
 // read.
 template <typename T, int TPR>
@@ -235,20 +262,12 @@ ce_bw_kernel(T *dz, const T *z, const int32_t *target, const float *lse, const f
 #pragma unroll
             for (int u = 0; u < kCeUnroll; ++u) {
                 const int64_t base = (c + (int64_t)u * TPR) * VV;
-                float f[VV];
-                Tr::unpack(raw[u], f);
-#pragma unroll
-                for (int e = 0; e < VV; ++e) f[e] = ce_grad(f[e], l2, g, base + e == tb);
-                st_stream16(db + base, Tr::pack(f));
+                st_stream16(db + base, ce_grad_vec<T>(raw[u], l2, g, tb - base));
             }
         }
         for (; c < nbody; c += TPR) {
             const int64_t base = c * VV;
-            float f[VV];
-            Tr::unpack(ld_stream16(zb + base), f);
-#pragma unroll
-            for (int e = 0; e < VV; ++e) f[e] = ce_grad(f[e], l2, g, base + e == tb);
-            st_stream16(db + base, Tr::pack(f));
+            st_stream16(db + base, ce_grad_vec<T>(ld_stream16(zb + base), l2, g, tb - base));
         }
     }
 }
