@@ -336,9 +336,9 @@ ln_dinp_vec(T *dx, const T *dy, const T *x, const T *gamma, const float *mean,
 // from one read of dy and x.  Block b owns rows [b*rpc, (b+1)*rpc) (a fixed
 // cut of the rows, independent of the GPU); its G row groups split them into
 // contiguous runs and stage dy and x as ln_dinp_vec does, while each thread
-// reads the row's mean and rstd into registers one row ahead (with a
-// per-thread 4-byte cp.async of them into the stage, as the input gradient
-// stages them, this kernel took 11-30 % longer at 768-2048 features).
+// reads the row's mean and rstd into registers one row ahead (staged with a
+// 4-byte cp.async by every thread, they made this kernel 11-30 % slower at
+// 768-2048 features).
 // Each thread also accumulates dgamma += dy * xhat and dbeta += dy for its
 // columns; the G groups' sums are added in group order through shared memory
 // and written as the chunk's partial part[(b*2 + {0,1}) * N + col], which
