@@ -614,7 +614,9 @@ def run_ours(args):
                                    "dependent launch, no event between them); per-kernel times "
                                    "from the same pass with an event pair around every call",
                        "l2": f"inputs larger than L2 (pass moves {step_bytes / 1e9:.2f} GB; "
-                             f"L2 {l2 / 1e6:.0f} MB); no flush"},
+                             f"L2 {l2 / 1e6:.0f} MB); no flush; each LayerNorm tensor "
+                             f"({ln_mb:.1f} MB) fits in L2, so the LayerNorm calls may find "
+                             f"their inputs warm from the call before; the cold tables flush"},
             "pct_of_peak": round(100 * value / world / peak, 2),
             "rows_per_s": {k: round(world * v * args.steps / job_s) for k, v in rows.items()},
             "bytes_per_step": step_bytes,
