@@ -350,8 +350,10 @@ def test_softmax_long_rows(dtype, Tk):
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
-@pytest.mark.parametrize("N", [1, 5, 64, 100, 770, 1000, 1536, 12288, 20000])
+@pytest.mark.parametrize("N", [1, 5, 8, 24, 32, 64, 100, 770, 1000, 1536, 12288, 20000])
 def test_layernorm_odd_widths(dtype, N):
+    # 8-32 features: rows of one to four 16-byte chunks, held by one or two
+    # threads (the row's shift and statistics pass through one-lane shuffles)
     check_layernorm(_ln_case(33, N, dtype), full=True)
 
 
@@ -745,7 +747,7 @@ def test_rmsnorm_small_configs():
 
 
 @pytest.mark.parametrize("dtype", ["f32", "f16", "bf16"])
-@pytest.mark.parametrize("N", [1, 7, 100, 770, 1536, 20000])
+@pytest.mark.parametrize("N", [1, 7, 8, 24, 32, 100, 770, 1536, 20000])
 def test_rmsnorm_odd_widths(dtype, N):
     check_rmsnorm(_ln_case(21, N, dtype), full=True)
 
@@ -817,7 +819,7 @@ def test_ln_bw_fused_small_configs_and_encoder():
 @pytest.mark.parametrize("dtype", ["f32", "f16", "bf16"])
 @pytest.mark.parametrize("rows,N", [(1, 64), (7, 1024), (303, 256), (304, 512), (305, 768),
                                     (1000, 2048), (333, 8192), (9, 16384), (21, 7), (21, 770),
-                                    (21, 20000)])
+                                    (21, 20000), (77, 8), (77, 24), (77, 32)])
 def test_ln_bw_fused_ragged_chunks_and_widths(dtype, rows, N):
     # row counts around the 304-chunk cut (one row per chunk, a ragged last
     # chunk) and widths that take the scalar two-kernel path
