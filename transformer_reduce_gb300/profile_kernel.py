@@ -6,7 +6,9 @@
 KERNEL is softmax_fw, softmax_bw, softmax_bw_masked, ln_fw, ln_dinp, ln_dgdb, ln_bw
 (the fused backward), rms_fw, rms_dinp, ce_fw or ce_bw (cross entropy; its
 workloads are the ce_* cases, ce_gpt2 by default), or pass: --launches whole
-passes of the encoder layer (the benchmark's ten calls on one stream).  Only the
+passes of the encoder layer (the benchmark's ten calls on one stream), or
+pass_fused: the same layer with the fused LayerNorm backward and the masked
+softmax backward (the benchmark's fused_pass).  Only the
 buffers that kernel touches are allocated (for the encoder workload at most
 ~0.8 GB), so a multi-pass ncu capture, which saves and restores device memory
 between passes, stays small while the tensors still exceed L2.
@@ -190,7 +192,8 @@ def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("kernel", nargs="?",
                     choices=["softmax_fw", "softmax_bw", "softmax_bw_masked", "ln_fw", "ln_dinp",
-                             "ln_dgdb", "ln_bw", "rms_fw", "rms_dinp", "ce_fw", "ce_bw", "pass"])
+                             "ln_dgdb", "ln_bw", "rms_fw", "rms_dinp", "ce_fw", "ce_bw", "pass",
+                             "pass_fused"])
     ap.add_argument("--workload", default="encoder_big",
                     help="softmax or LayerNorm case name (encoder_big picks the encoder's case)")
     ap.add_argument("--launches", type=int, default=3)
@@ -230,15 +233,15 @@ def main(argv=None):
         return
     if a.kernel is None:
         ap.error("KERNEL or --sweep is required")
-    if a.kernel == "pass":
+    if a.kernel in ("pass", "pass_fused"):
         from .layer_path import LayerReducePath
         path = LayerReducePath(workloads.ENCODER_BIG["softmax"],
                                workloads.ENCODER_BIG["layernorm"], device=dev)
         torch.cuda.synchronize(dev)
         for _ in range(a.launches):
-            path.run()
+            path.run() if a.kernel == "pass" else path.run_fused()
         torch.cuda.synchronize(dev)
-        print(f"profile_kernel: {a.launches} encoder passes")
+        print(f"profile_kernel: {a.launches} encoder passes ({a.kernel})")
         return
     if a.kernel.startswith("ce"):
         case = CE_CASES[a.workload if a.workload in CE_CASES else "ce_gpt2"]
